@@ -1,0 +1,305 @@
+/*
+ * oracle.c -- plain CPU reference for the W4A16 fused matrix multiply
+ *             Y = X . dequant(W)
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+ * calls this file; only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg do.  It shares no code, header, table or constant with the
+ * CUDA library.
+ *
+ * What it follows (pages on Marlin, cited by title and section):
+ *   - "Marlin / GPTQ-Marlin" (brain.gartu.xyz), section "Le probleme": each
+ *     linear layer computes Y = X_fp16 x W_int4, dequantising the INT4 weights
+ *     to FP16 on the fly before the multiply.
+ *   - "Marlin" (dingiv.github.io), section "Group size": one scale (and one
+ *     zero point) per group of 128 consecutive weights.
+ *   - same page, section "dequant precision": INT4 -> FP16 is exact (FP16 holds
+ *     all 16 values), the multiply accumulates in FP32 and the output is FP16.
+ *
+ * The oracle computes the plain definition, with no blocking or reordering:
+ *   1. q[k][n] = nibble (k mod 8) of Qp[k/8][n]                 (GPTQ order)
+ *   2. z[j][n] = nibble (n mod 8) of Zp[j][n/8], or 8 when no zeros are given
+ *   3. w[k][n] = fp16_rne( (q - z) * s[k/g][n] )   -- one rounding, exact
+ *                product taken in double (|q-z| <= 15 times an fp16 value is
+ *                exact in binary64)
+ *   4. y[m][n] = sum_k x[m][k] * w[k][n], in binary64, k ascending
+ * plus the tile layout of the repacked weights (the "reshuffle" of the pages:
+ * "Marlin / GPTQ-Marlin", section "Tiled layout et repacking"; "Marlin Project
+ * Overview" (vecbase.com), section "Key Techniques", item "Reshuffling").  The
+ * repacked layout is this library's own; its index formula is:
+ *   word index  = ((nt * (K/64) + kb) * 2 + h) * 512 + nl * 4 + i
+ *   holds the 8 codes  q[kb*64 + (h*4+i)*8 + koff(p)][nt*128 + nl],  p = 0..7,
+ *   code of nibble position p at bits 4p..4p+3, where koff(p) = 2p for p < 4
+ *   and 2(p-4)+1 for p >= 4.
+ *
+ * Build: gcc -O2 -ffp-contract=off -fPIC -shared -pthread (no FMA contraction,
+ * so every sum rounds after each add, identically on x86-64 and aarch64).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---- IEEE-754 binary16 <-> binary64 (own bit-level routines) ----------- */
+
+/* Exact value of a binary16 bit pattern. */
+double oracle_half_to_double(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int e = (h >> 10) & 0x1F;
+  int f = h & 0x3FF;
+  double v;
+  if (e == 0x1F) {
+    v = f ? NAN : INFINITY;
+  } else if (e == 0) {
+    v = ldexp((double)f, -24); /* subnormal: f * 2^-24 */
+  } else {
+    v = ldexp((double)(1024 + f), e - 25); /* (1024+f) * 2^(e-15-10) */
+  }
+  return sign ? -v : v;
+}
+
+/* Round a binary64 value to the nearest binary16, ties to even, with
+ * gradual underflow and overflow to infinity.  Every step below is exact in
+ * binary64 except rint(), which performs the single round-to-nearest-even. */
+uint16_t oracle_double_to_half_rne(double v) {
+  if (isnan(v)) return 0x7E00;
+  uint16_t sign = signbit(v) ? 0x8000 : 0;
+  double a = fabs(v);
+  if (a == 0.0) return sign;
+  /* 65504 is the largest finite half; 65520 is the midpoint to 2^16 and rounds
+   * to the even neighbour 2^16, i.e. overflows. */
+  if (a >= 65520.0) return sign | 0x7C00;
+  int E;
+  frexp(a, &E);            /* a = f * 2^E, f in [0.5, 1) */
+  int e = E - 1;           /* a in [2^e, 2^(e+1)) */
+  if (e < -14) {           /* subnormal range: quantum 2^-24 */
+    double n = rint(ldexp(a, 24));
+    return sign | (uint16_t)n; /* n == 1024 is the smallest normal, 0x0400 */
+  }
+  double n = rint(ldexp(a, 10 - e)); /* in [1024, 2048] */
+  if (n >= 2048.0) { n = 1024.0; e += 1; }
+  if (e > 15) return sign | 0x7C00;
+  return sign | (uint16_t)(((e + 15) << 10) | ((int)n - 1024));
+}
+
+/* ---- steps 1-3: unpack and dequantise ---------------------------------- */
+
+static inline int code_at(const int32_t* Qp, int N, int k, int n) {
+  uint32_t word = (uint32_t)Qp[(size_t)(k / 8) * N + n];
+  return (int)((word >> (4 * (k % 8))) & 0xFu);
+}
+
+static inline int zero_at(const int32_t* Zp, int N, int j, int n) {
+  if (!Zp) return 8;
+  uint32_t word = (uint32_t)Zp[(size_t)j * (N / 8) + n / 8];
+  return (int)((word >> (4 * (n % 8))) & 0xFu);
+}
+
+/* q[k*N + n] for k < K, n < N. */
+int oracle_unpack_codes(const int32_t* Qp, int K, int N, uint8_t* q) {
+  if (K % 8 || K <= 0 || N <= 0) return 1;
+  for (int k = 0; k < K; ++k)
+    for (int n = 0; n < N; ++n) q[(size_t)k * N + n] = (uint8_t)code_at(Qp, N, k, n);
+  return 0;
+}
+
+/* z[j*N + n] for j < G, n < N (8 everywhere when Zp is NULL). */
+int oracle_unpack_zeros(const int32_t* Zp, int G, int N, uint8_t* z) {
+  if (G <= 0 || N % 8) return 1;
+  for (int j = 0; j < G; ++j)
+    for (int n = 0; n < N; ++n) z[(size_t)j * N + n] = (uint8_t)zero_at(Zp, N, j, n);
+  return 0;
+}
+
+/* w = fp16_rne((q - z) * s) for one weight. */
+static inline uint16_t dequant_one(int q, int z, uint16_t s_bits) {
+  double prod = (double)(q - z) * oracle_half_to_double(s_bits);
+  return oracle_double_to_half_rne(prod);
+}
+
+uint16_t oracle_dequant_scalar(int q, int z, uint16_t s_bits) { return dequant_one(q, z, s_bits); }
+
+/* W[k*N + n] (fp16 bits) = dequant of the whole K x N matrix.
+ * S is [K/g][N] fp16 bits, Zp is [K/g][N/8] packed zeros or NULL. */
+int oracle_dequant(const int32_t* Qp, const uint16_t* S, const int32_t* Zp, int K, int N, int g,
+                   uint16_t* W) {
+  if (K % 8 || N % 8 || g <= 0 || K % g) return 1;
+  for (int k = 0; k < K; ++k) {
+    int j = k / g;
+    for (int n = 0; n < N; ++n)
+      W[(size_t)k * N + n] = dequant_one(code_at(Qp, N, k, n), zero_at(Zp, N, j, n),
+                                         S[(size_t)j * N + n]);
+  }
+  return 0;
+}
+
+/* ---- step 4: fp64 matrix multiply --------------------------------------- */
+
+typedef struct {
+  const uint16_t* X;
+  const uint16_t* W;
+  int M, K, N, n0, n1;
+  double* Y;
+} gemm_job;
+
+static void* gemm_worker(void* arg) {
+  gemm_job* j = (gemm_job*)arg;
+  int K = j->K, N = j->N;
+  double* wcol = (double*)malloc(sizeof(double) * K);
+  for (int n = j->n0; n < j->n1; ++n) {
+    for (int k = 0; k < K; ++k) wcol[k] = oracle_half_to_double(j->W[(size_t)k * N + n]);
+    for (int m = 0; m < j->M; ++m) {
+      const uint16_t* x = j->X + (size_t)m * K;
+      double acc = 0.0;
+      for (int k = 0; k < K; ++k) acc += oracle_half_to_double(x[k]) * wcol[k];
+      j->Y[(size_t)m * N + n] = acc;
+    }
+  }
+  free(wcol);
+  return NULL;
+}
+
+/* Y[m*N + n] = sum_k X[m][k] * W[k][n] in binary64, k ascending.
+ * Threads split the columns; each column's sums are the same whatever the
+ * thread count. */
+int oracle_gemm(const uint16_t* X, const uint16_t* W, int M, int K, int N, double* Y, int nthreads) {
+  if (M < 0 || K <= 0 || N <= 0) return 1;
+  if (M == 0) return 0;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > N) nthreads = N;
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * nthreads);
+  gemm_job* jobs = (gemm_job*)malloc(sizeof(gemm_job) * nthreads);
+  for (int t = 0; t < nthreads; ++t) {
+    jobs[t] = (gemm_job){X, W, M, K, N, (int)((long long)N * t / nthreads),
+                         (int)((long long)N * (t + 1) / nthreads), Y};
+    pthread_create(&th[t], NULL, gemm_worker, &jobs[t]);
+  }
+  for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+  free(th);
+  free(jobs);
+  return 0;
+}
+
+/* ---- the whole definition, straight from the packed inputs ------------- */
+
+typedef struct {
+  const uint16_t* X;
+  const int32_t* Qp;
+  const uint16_t* S;
+  const int32_t* Zp;
+  int M, K, N, g;
+  const int64_t* idx; /* flat indices m*N + n; NULL = every entry */
+  int64_t i0, i1;
+  double* out;
+} w4a16_job;
+
+/* y[m][n] for one (m, n): dequantise column n (steps 1-3) and sum (step 4). */
+static double entry(const w4a16_job* j, int m, int n) {
+  const uint16_t* x = j->X + (size_t)m * j->K;
+  double acc = 0.0;
+  for (int k = 0; k < j->K; ++k) {
+    int grp = k / j->g;
+    uint16_t w = dequant_one(code_at(j->Qp, j->N, k, n), zero_at(j->Zp, j->N, grp, n),
+                             j->S[(size_t)grp * j->N + n]);
+    acc += oracle_half_to_double(x[k]) * oracle_half_to_double(w);
+  }
+  return acc;
+}
+
+static void* w4a16_worker(void* arg) {
+  w4a16_job* j = (w4a16_job*)arg;
+  if (j->idx) {
+    for (int64_t i = j->i0; i < j->i1; ++i) {
+      int64_t f = j->idx[i];
+      j->out[i] = entry(j, (int)(f / j->N), (int)(f % j->N));
+    }
+  } else {
+    /* whole rows of columns: i indexes columns n, all m */
+    for (int64_t n = j->i0; n < j->i1; ++n)
+      for (int m = 0; m < j->M; ++m) j->out[(size_t)m * j->N + n] = entry(j, m, (int)n);
+  }
+  return NULL;
+}
+
+/* Y (or the listed entries) of Y = X . dequant(W), computed from the packed
+ * GPTQ-order inputs.  idx == NULL: out is [M][N]; else out[i] = y at flat
+ * index idx[i] = m*N + n. */
+int oracle_w4a16(const uint16_t* X, const int32_t* Qp, const uint16_t* S, const int32_t* Zp, int M,
+                 int K, int N, int g, const int64_t* idx, int64_t count, double* out, int nthreads) {
+  if (M < 0 || K <= 0 || N <= 0 || K % 8 || N % 8 || g <= 0 || K % g) return 1;
+  if (M == 0) return 0;
+  int64_t total = idx ? count : N;
+  if (total <= 0) return 0;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > total) nthreads = (int)total;
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * nthreads);
+  w4a16_job* jobs = (w4a16_job*)malloc(sizeof(w4a16_job) * nthreads);
+  for (int t = 0; t < nthreads; ++t) {
+    jobs[t] = (w4a16_job){X, Qp, S, Zp, M, K, N, g, idx, total * t / nthreads,
+                          total * (t + 1) / nthreads, out};
+    pthread_create(&th[t], NULL, w4a16_worker, &jobs[t]);
+  }
+  for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+  free(th);
+  free(jobs);
+  return 0;
+}
+
+/* ---- repacked tile layout ------------------------------------------------ */
+
+/* k offset, within a group of 8 consecutive k, of the code stored at nibble
+ * position p of a repacked word. */
+static inline int koff(int p) { return p < 4 ? 2 * p : 2 * (p - 4) + 1; }
+
+/* Qp [K/8][N] GPTQ order -> P [(N/128)*(K/64)*1024] words, tile layout. */
+int oracle_repack(const int32_t* Qp, int K, int N, int32_t* P) {
+  if (K <= 0 || N <= 0 || K % 64 || N % 128) return 1;
+  int KB = K / 64, NT = N / 128;
+  for (int nt = 0; nt < NT; ++nt)
+    for (int kb = 0; kb < KB; ++kb)
+      for (int h = 0; h < 2; ++h)
+        for (int nl = 0; nl < 128; ++nl)
+          for (int i = 0; i < 4; ++i) {
+            uint32_t word = 0;
+            for (int p = 0; p < 8; ++p) {
+              int k = kb * 64 + (h * 4 + i) * 8 + koff(p);
+              word |= (uint32_t)code_at(Qp, N, k, nt * 128 + nl) << (4 * p);
+            }
+            size_t at = ((size_t)(nt * KB + kb) * 2 + h) * 512 + (size_t)nl * 4 + i;
+            P[at] = (int32_t)word;
+          }
+  return 0;
+}
+
+/* Inverse of oracle_repack: tile layout -> GPTQ order. */
+int oracle_unrepack(const int32_t* P, int K, int N, int32_t* Qp) {
+  if (K <= 0 || N <= 0 || K % 64 || N % 128) return 1;
+  int KB = K / 64, NT = N / 128;
+  memset(Qp, 0, sizeof(int32_t) * (size_t)(K / 8) * N);
+  for (int nt = 0; nt < NT; ++nt)
+    for (int kb = 0; kb < KB; ++kb)
+      for (int h = 0; h < 2; ++h)
+        for (int nl = 0; nl < 128; ++nl)
+          for (int i = 0; i < 4; ++i) {
+            size_t at = ((size_t)(nt * KB + kb) * 2 + h) * 512 + (size_t)nl * 4 + i;
+            uint32_t word = (uint32_t)P[at];
+            for (int p = 0; p < 8; ++p) {
+              int k = kb * 64 + (h * 4 + i) * 8 + koff(p);
+              int n = nt * 128 + nl;
+              uint32_t q = (word >> (4 * p)) & 0xFu;
+              Qp[(size_t)(k / 8) * N + n] |= (int32_t)(q << (4 * (k % 8)));
+            }
+          }
+  return 0;
+}
+
+/* Element-wise fp16_rne of n binary64 values (bits out). */
+void oracle_round_array(const double* v, int64_t n, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_double_to_half_rne(v[i]);
+}
+
+/* Element-wise exact value of n binary16 bit patterns. */
+void oracle_widen_array(const uint16_t* h, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_half_to_double(h[i]);
+}
