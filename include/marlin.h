@@ -1,0 +1,141 @@
+/*
+ * marlin.h -- C ABI of the GB300 (sm_103a) W4A16 fused matrix multiply
+ *
+ *     Y[M][N] = X[M][K] . dequant(W)[K][N],   dequant(w) = fp16((q - z) * s)
+ *
+ * The operation is the one the Marlin pages define: "Marlin / GPTQ-Marlin"
+ * (brain.gartu.xyz), section "Le probleme": every linear layer computes
+ * Y = X_fp16 x W_int4, the INT4 weights dequantised to FP16 on the fly;
+ * "Marlin" (dingiv.github.io), section "Group size": one fp16 scale (and one
+ * zero point) per group of 128 consecutive K elements of a column; section
+ * "dequant precision": FP16 operands, FP32 accumulation, FP16 output.
+ *
+ * Conventions for every entry point
+ *   - Device pointers are CUDA device addresses on the current device; host
+ *     pointers are marked "host".  The caller owns and allocates every buffer;
+ *     the library allocates no device memory.
+ *   - Every call is asynchronous on `stream` (0 = legacy default stream) unless
+ *     stated otherwise, and never synchronises, except
+ *     marlin_last_device_status.
+ *   - Argument errors are detected on the host before anything is launched; the
+ *     call then returns the error code and touches nothing.
+ *   - fp16 data is passed as raw 16-bit IEEE-754 binary16 (`uint16_t`).
+ *
+ * Data formats
+ *   X       fp16 [M][K], row-major (K contiguous), 16-byte aligned base.
+ *   q       GPTQ order: int32 [K/8][N]; bits 4i..4i+3 of word [r][n] hold the
+ *           code q[8r+i][n], q in 0..15.
+ *   scales  fp16 [K/group][N] (row j = group j).
+ *   zeros   int32 [K/group][N/8]; bits 4j..4j+3 of word [g][c] hold z[g][8c+j]
+ *           (stored literally, no offset).  NULL means z = 8 everywhere.
+ *   group   128, any multiple of 128 that divides K, or K (or -1 meaning K)
+ *           for one scale per column.
+ *   Shapes  K % 128 == 0, N % 128 == 0, M >= 0 (M == 0 is a no-op).
+ */
+#ifndef W4A16_GB300_MARLIN_H
+#define W4A16_GB300_MARLIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* marlin_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  MARLIN_OK = 0,
+  MARLIN_ERR_INVALID_ARG = 1,          /* bad shape, group, NULL pointer          */
+  MARLIN_ERR_UNSUPPORTED = 2,          /* valid request this build cannot serve   */
+  MARLIN_ERR_MISALIGNED = 3,           /* a pointer is not 16-byte aligned        */
+  MARLIN_ERR_WORKSPACE_TOO_SMALL = 4,  /* workspace smaller than required        */
+  MARLIN_ERR_CUDA = 5,                 /* a CUDA runtime call or launch failed    */
+  MARLIN_ERR_TIMEOUT = 6               /* a bounded wait inside a kernel gave up  */
+} marlin_status_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* marlin_status_string(marlin_status_t status);
+
+/*
+ * Size and offsets of the single repacked weight buffer, laid out as
+ * [codes | scales | zeros]:
+ *   codes  K*N/2 bytes in this library's tile layout (see marlin_repack);
+ *   scales fp16 [K/group][N], verbatim, at *off_scales;
+ *   zeros  int32 [K/group][N/8], verbatim, at *off_zeros (only if has_zeros;
+ *          *off_zeros = *bytes otherwise).
+ * All offsets are multiples of 256 bytes.  Host-only, no CUDA call.
+ * bytes, off_scales, off_zeros: host pointers, each may be NULL.
+ */
+marlin_status_t marlin_packed_layout(int K, int N, int group, int has_zeros, size_t* bytes,
+                                     size_t* off_scales, size_t* off_zeros);
+
+/*
+ * Offline repack ("reshuffle" of the weights into a tile layout, done once at
+ * load time): "Marlin / GPTQ-Marlin", section "Tiled layout et repacking";
+ * "Marlin Project Overview" (vecbase.com), section "Key Techniques", item
+ * "Reshuffling".
+ *
+ * q       device, int32 [K/8][N] GPTQ order (read only).
+ * scales  device, fp16 [K/group][N] (read only).
+ * zeros   device, int32 [K/group][N/8], or NULL for z = 8 (read only).
+ * out     device, marlin_packed_layout(K, N, group, zeros != NULL) bytes,
+ *         16-byte aligned, written.  Must not overlap the inputs.
+ * Code layout in `out` (32-bit words):
+ *   word ((nt*(K/64) + kb)*2 + h)*512 + nl*4 + i holds, at bits 4p..4p+3
+ *   (p = 0..7), the code q[kb*64 + (h*4+i)*8 + koff(p)][nt*128 + nl] with
+ *   koff(p) = 2p for p < 4 and 2(p-4)+1 for p >= 4.
+ * Errors: INVALID_ARG (shape/group/NULL), MISALIGNED, CUDA (launch).
+ */
+marlin_status_t marlin_repack(const int32_t* q, const uint16_t* scales, const int32_t* zeros, int K,
+                              int N, int group, void* out, marlin_stream_t stream);
+
+/*
+ * Bytes of device workspace marlin_gemm needs for this problem on `device`
+ * (its SM count sets the partition).  The workspace holds the fp32 partial
+ * tiles of the striped partition's global reduction, one arrival counter per
+ * output tile and a status word.  A buffer sized for M also serves every
+ * smaller M with the same K, N, group.  Host-only; queries the device
+ * attributes once.  bytes: host pointer, written.
+ */
+marlin_status_t marlin_workspace_bytes(int M, int K, int N, int group, int device, size_t* bytes);
+
+/*
+ * The fused W4A16 matrix multiply: Y = X . dequant(W) with fp32 accumulation
+ * and fp16 output (round to nearest even; overflow gives +-inf).
+ * "Marlin / GPTQ-Marlin", sections "Le probleme" and "Architecture generale"
+ * (one kernel fuses the dequantisation and the GEMM); "Marlin Project
+ * Overview", section "Key Techniques", item "Striped Partitioning" (the SM
+ * partition with global reduction).
+ *
+ * X          device, fp16 [M][K] row-major, 16-byte aligned (read only).
+ * packed     device, the codes region of a marlin_repack output (offset 0).
+ * scales     device, fp16 [K/group][N] (normally packed + off_scales).
+ * zeros      device, int32 [K/group][N/8] (packed + off_zeros) or NULL (z = 8).
+ * Y          device, fp16 [M][N] row-major, written; must not overlap inputs.
+ * workspace  device, >= marlin_workspace_bytes(...) bytes, 16-byte aligned.
+ *            Zero it once after allocating; every call leaves it zeroed again.
+ *            Calls that share a workspace must be ordered (same stream, or
+ *            events): concurrent calls on one workspace race.
+ * Result is deterministic: the same inputs give bit-identical Y on every run.
+ * Errors: INVALID_ARG, MISALIGNED, WORKSPACE_TOO_SMALL (host checks, nothing
+ * launched); CUDA (launch failure).  A bounded wait that expires inside the
+ * kernel is reported later by marlin_last_device_status.
+ */
+marlin_status_t marlin_gemm(const uint16_t* X, const void* packed, const uint16_t* scales,
+                            const int32_t* zeros, uint16_t* Y, int M, int K, int N, int group,
+                            void* workspace, size_t workspace_bytes, marlin_stream_t stream);
+
+/*
+ * Synchronises `stream`, reads and clears the device status word that
+ * marlin_gemm keeps in `workspace`, and returns MARLIN_OK or
+ * MARLIN_ERR_TIMEOUT (a bounded wait in a kernel expired; that call's Y is
+ * not valid).  workspace: device, as passed to marlin_gemm.
+ */
+marlin_status_t marlin_last_device_status(void* workspace, marlin_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_GB300_MARLIN_H */

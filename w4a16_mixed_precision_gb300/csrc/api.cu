@@ -1,0 +1,250 @@
+// api.cu -- the C ABI declared in include/marlin.h: argument checks, the
+// partition plan, the X tensor map, and the kernel launches.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "kernels.h"
+#include "marlin.h"
+
+using namespace w4a16;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
+
+struct DeviceState {
+  bool init = false;
+  int sms = 0;
+  int smem_optin = 0;
+  bool smem_set = false;
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+marlin_status_t device_state(int device, DeviceState** out) {
+  if (device < 0 || device >= kMaxDevices) return MARLIN_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& d = g_dev[device];
+  if (!d.init) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) !=
+            cudaSuccess)
+      return MARLIN_ERR_CUDA;
+    d.init = true;
+  }
+  *out = &d;
+  return MARLIN_OK;
+}
+
+marlin_status_t get_encoder() {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_encode) return MARLIN_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return MARLIN_ERR_CUDA;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return MARLIN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// group -1 means K; otherwise a positive multiple of 128 dividing K.
+bool normalise_group(int K, int* group) {
+  if (*group == -1) *group = K;
+  return *group > 0 && *group % 128 == 0 && K % *group == 0;
+}
+
+bool valid_shape(int K, int N) { return K > 0 && N > 0 && K % 128 == 0 && N % 128 == 0; }
+
+// The partition plan.  bn = tokens per m-tile (UMMA N, multiple of 16, <= 256);
+// a unit is one (m-tile, 128-column tile, K slice of cpu*64); the grid is one
+// CTA per SM (fewer if there are fewer units), each taking an equal stripe.
+GemmPlan make_plan(int M, int K, int N, int sms, int smem_optin, bool has_zeros) {
+  GemmPlan g{};
+  g.bn = M <= kMaxBn ? (int)round_up((size_t)M, 16) : kMaxBn;
+  if (g.bn < 16) g.bn = 16;
+  g.m_tiles = (M + g.bn - 1) / g.bn;
+  g.n_tiles = N / kTileN;
+  g.cpu = g.bn <= 64 ? 2 : 1;
+  g.kt = K / (kChunkK * g.cpu);
+  g.units = (long long)g.m_tiles * g.n_tiles * g.kt;
+  g.grid = (int)(g.units < sms ? g.units : sms);
+  const size_t x_chunk = (size_t)g.bn * 128;
+  size_t stage = g.cpu * (x_chunk + kChunkCodeBytes) + kTileN * 2 + (has_zeros ? kTileN / 2 : 0);
+  g.stage_bytes = (uint32_t)round_up(stage, 1024);
+  const int budget = smem_optin - kCtrlBytes - 1024;  // control block + alignment slack
+  int stages = budget / (int)g.stage_bytes;
+  if (stages > kMaxStages) stages = kMaxStages;
+  g.stages = stages;
+  g.smem_bytes = (uint32_t)(kCtrlBytes + 1024 + (size_t)stages * g.stage_bytes);
+  // workspace: [status 256 B][counters][partials]
+  g.ws_counters_off = 256;
+  g.ws_partials_off = round_up(g.ws_counters_off + sizeof(int) * (size_t)g.m_tiles * g.n_tiles, 256);
+  g.ws_bytes = g.ws_partials_off + (size_t)sms * 2 * g.bn * kTileN * sizeof(float);
+  return g;
+}
+
+marlin_status_t current_device(int* dev) {
+  return cudaGetDevice(dev) == cudaSuccess ? MARLIN_OK : MARLIN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* marlin_status_string(marlin_status_t s) {
+  switch (s) {
+    case MARLIN_OK: return "MARLIN_OK";
+    case MARLIN_ERR_INVALID_ARG: return "MARLIN_ERR_INVALID_ARG";
+    case MARLIN_ERR_UNSUPPORTED: return "MARLIN_ERR_UNSUPPORTED";
+    case MARLIN_ERR_MISALIGNED: return "MARLIN_ERR_MISALIGNED";
+    case MARLIN_ERR_WORKSPACE_TOO_SMALL: return "MARLIN_ERR_WORKSPACE_TOO_SMALL";
+    case MARLIN_ERR_CUDA: return "MARLIN_ERR_CUDA";
+    case MARLIN_ERR_TIMEOUT: return "MARLIN_ERR_TIMEOUT";
+  }
+  return "MARLIN_ERR_UNKNOWN";
+}
+
+marlin_status_t marlin_packed_layout(int K, int N, int group, int has_zeros, size_t* bytes,
+                                     size_t* off_scales, size_t* off_zeros) {
+  if (!valid_shape(K, N) || !normalise_group(K, &group)) return MARLIN_ERR_INVALID_ARG;
+  const size_t G = (size_t)(K / group);
+  const size_t codes = (size_t)K * N / 2;
+  const size_t sc = round_up(codes, 256);
+  const size_t zo = round_up(sc + G * N * 2, 256);
+  const size_t total = has_zeros ? zo + G * N / 2 : zo;
+  if (bytes) *bytes = total;
+  if (off_scales) *off_scales = sc;
+  if (off_zeros) *off_zeros = has_zeros ? zo : total;
+  return MARLIN_OK;
+}
+
+marlin_status_t marlin_repack(const int32_t* q, const uint16_t* scales, const int32_t* zeros, int K,
+                              int N, int group, void* out, marlin_stream_t stream) {
+  if (!q || !scales || !out) return MARLIN_ERR_INVALID_ARG;
+  if (!valid_shape(K, N) || !normalise_group(K, &group)) return MARLIN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(scales) || !aligned16(out) || (zeros && !aligned16(zeros)))
+    return MARLIN_ERR_MISALIGNED;
+  size_t bytes, off_s, off_z;
+  marlin_packed_layout(K, N, group, zeros != nullptr, &bytes, &off_s, &off_z);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* o = static_cast<uint8_t*>(out);
+  const size_t G = (size_t)(K / group);
+  if (launch_repack(reinterpret_cast<const uint32_t*>(q), reinterpret_cast<uint32_t*>(o), K, N, st) !=
+      cudaSuccess)
+    return MARLIN_ERR_CUDA;
+  if (launch_copy16(scales, o + off_s, G * N * 2, st) != cudaSuccess) return MARLIN_ERR_CUDA;
+  if (zeros && launch_copy16(zeros, o + off_z, G * N / 2, st) != cudaSuccess) return MARLIN_ERR_CUDA;
+  return MARLIN_OK;
+}
+
+marlin_status_t marlin_workspace_bytes(int M, int K, int N, int group, int device, size_t* bytes) {
+  if (!bytes || M < 0 || !valid_shape(K, N) || !normalise_group(K, &group))
+    return MARLIN_ERR_INVALID_ARG;
+  DeviceState* d;
+  marlin_status_t s = device_state(device, &d);
+  if (s != MARLIN_OK) return s;
+  const GemmPlan g = make_plan(M > 0 ? M : 1, K, N, d->sms, d->smem_optin, true);
+  *bytes = g.ws_bytes;
+  return MARLIN_OK;
+}
+
+marlin_status_t marlin_gemm(const uint16_t* X, const void* packed, const uint16_t* scales,
+                            const int32_t* zeros, uint16_t* Y, int M, int K, int N, int group,
+                            void* workspace, size_t workspace_bytes, marlin_stream_t stream) {
+  if (M < 0 || !valid_shape(K, N) || !normalise_group(K, &group)) return MARLIN_ERR_INVALID_ARG;
+  if (M == 0) return MARLIN_OK;
+  if (!X || !packed || !scales || !Y || !workspace) return MARLIN_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(packed) || !aligned16(scales) || (zeros && !aligned16(zeros)) ||
+      !aligned16(workspace) || (reinterpret_cast<uintptr_t>(Y) & 1u))
+    return MARLIN_ERR_MISALIGNED;
+  int dev;
+  marlin_status_t s = current_device(&dev);
+  if (s != MARLIN_OK) return s;
+  DeviceState* d;
+  if ((s = device_state(dev, &d)) != MARLIN_OK) return s;
+  if ((s = get_encoder()) != MARLIN_OK) return s;
+
+  const GemmPlan g = make_plan(M, K, N, d->sms, d->smem_optin, zeros != nullptr);
+  if (g.stages < 2) return MARLIN_ERR_UNSUPPORTED;
+  if (workspace_bytes < g.ws_bytes) return MARLIN_ERR_WORKSPACE_TOO_SMALL;
+
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!d->smem_set) {
+      if (gemm_set_smem_limit(d->smem_optin) != cudaSuccess) return MARLIN_ERR_CUDA;
+      d->smem_set = true;
+    }
+  }
+
+  CUtensorMap x_map;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kChunkK, (cuuint32_t)g.bn};
+  const cuuint32_t estr[2] = {1, 1};
+  if (g_encode(&x_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(X), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return MARLIN_ERR_CUDA;
+
+  GemmParams p{};
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.codes = static_cast<const uint32_t*>(packed);
+  p.scales = scales;
+  p.zeros = reinterpret_cast<const uint8_t*>(zeros);
+  p.Y = Y;
+  p.status = reinterpret_cast<int*>(ws);
+  p.counters = reinterpret_cast<int*>(ws + g.ws_counters_off);
+  p.partials = reinterpret_cast<float*>(ws + g.ws_partials_off);
+  p.M = M;
+  p.K = K;
+  p.N = N;
+  p.group = group;
+  p.bn = g.bn;
+  p.m_tiles = g.m_tiles;
+  p.n_tiles = g.n_tiles;
+  p.kt = g.kt;
+  p.cpu = g.cpu;
+  p.units = g.units;
+  p.stages = g.stages;
+  p.stage_bytes = g.stage_bytes;
+  p.x_chunk_bytes = (uint32_t)g.bn * 128;
+  p.off_codes = (uint32_t)g.cpu * p.x_chunk_bytes;
+  p.off_scales = p.off_codes + (uint32_t)g.cpu * kChunkCodeBytes;
+  p.off_zeros = p.off_scales + kTileN * 2;
+  p.tx_bytes = (uint32_t)g.cpu * (p.x_chunk_bytes + kChunkCodeBytes) + kTileN * 2 +
+               (zeros ? kTileN / 2 : 0);
+  p.weights_reused = g.m_tiles > 1;
+  p.timeout_ns = kDefaultTimeoutNs;
+  if (launch_gemm(x_map, p, g.grid, g.smem_bytes, reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return MARLIN_ERR_CUDA;
+  return MARLIN_OK;
+}
+
+marlin_status_t marlin_last_device_status(void* workspace, marlin_stream_t stream) {
+  if (!workspace) return MARLIN_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MARLIN_ERR_CUDA;
+  int status = 0;
+  if (cudaMemcpy(&status, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MARLIN_ERR_CUDA;
+  if (status != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(workspace, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return MARLIN_ERR_CUDA;
+    return MARLIN_ERR_TIMEOUT;
+  }
+  return MARLIN_OK;
+}
+
+}  // extern "C"

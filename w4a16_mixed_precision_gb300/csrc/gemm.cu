@@ -1,0 +1,457 @@
+// gemm.cu -- the fused W4A16 matrix multiply for GB300 (sm_103a).
+//
+// Computes Y[M][N] = X[M][K] . dequant(W)[K][N], dequant(w) = fp16((q - z) * s)
+// ("Marlin / GPTQ-Marlin", section "Le probleme"; "Marlin" (dingiv.github.io),
+// sections "Group size" and "dequant precision").
+//
+// Design (Blackwell-first; the pages' Ampere kernel is prior art only):
+//   * Swapped operands: the tensor core computes D[n][m] = sum_k Wt[n][k] X[m][k]
+//     with UMMA M = 128 output columns n and UMMA N = bn tokens m (16..256), so a
+//     decode batch of 1..16 tokens still fills the 128-row MMA.
+//   * One persistent CTA per SM walks a contiguous stripe of work units
+//     (m-tile, n-tile, K-slice) -- the pages' "striped partitioning"
+//     ("Marlin Project Overview", section "Key Techniques").  Column tiles cut by
+//     a stripe boundary are summed through an fp32 workspace by the last CTA to
+//     arrive, in a fixed order, so results are bit-reproducible.
+//   * Warp roles: warp 0 streams packed codes, scales, zeros (bulk TMA) and X
+//     (tensor TMA, 128-byte swizzle) through a multi-stage mbarrier ring in shared
+//     memory ("Marlin", section "async copy and pipeline"); warps 4..11 (two
+//     warpgroups, alternating chunks) turn 4-bit codes into fp16 with the
+//     0x6400 exponent trick, scale them with one fp16 multiply, and store the
+//     result straight into tensor memory as the A operand; warp 1 issues
+//     tcgen05.mma (A from TMEM, B = X from shared memory, fp32 accumulators in
+//     TMEM); the dequant warps then read the accumulators back with tcgen05.ld
+//     and write fp16 Y (or fp32 partials).
+//   * Every wait is bounded (global timer); on expiry the kernel records
+//     kStatusTimeout in the status word, drains its own copies and MMAs, frees
+//     TMEM and returns.
+#include <cuda_fp16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace w4a16 {
+
+namespace {
+
+struct Ctrl {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t afull[kAStages];
+  uint64_t aempty[kAStages];
+  uint64_t dfull;
+  uint64_t dempty;
+  uint64_t drain;
+  uint64_t red_arrive;  // dequant warps -> reducer leader: partial tile stored
+  uint64_t red_go;      // leader -> dequant warps: arrival counted
+  uint32_t tmem_base;
+  int abort;
+  int reduce_last;
+};
+static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
+
+constexpr int kNumDqWarps = 8;
+constexpr int kFirstDqWarp = 4;
+
+// ---- bounded waits ----------------------------------------------------------
+
+__device__ __forceinline__ void raise_timeout(Ctrl* c, const GemmParams& p) {
+  *reinterpret_cast<volatile int*>(&c->abort) = 1;
+  atomicOr(p.status, kStatusTimeout);
+}
+
+// Single-thread wait.  Returns false when the CTA is aborting or the wait expired.
+__device__ bool wait_thread(uint32_t bar, uint32_t parity, Ctrl* c, const GemmParams& p) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = global_timer_ns();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*reinterpret_cast<volatile int*>(&c->abort)) return false;
+    if (global_timer_ns() - t0 > p.timeout_ns) {
+      raise_timeout(c, p);
+      return false;
+    }
+  }
+}
+
+// Whole-warp wait with a warp-uniform outcome.
+__device__ bool wait_warp(uint32_t bar, uint32_t parity, Ctrl* c, const GemmParams& p) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  const uint32_t lane = threadIdx.x & 31;
+  uint64_t t0 = global_timer_ns();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    int stop = 0;
+    if (lane == 0) {
+      if (*reinterpret_cast<volatile int*>(&c->abort)) {
+        stop = 1;
+      } else if (global_timer_ns() - t0 > p.timeout_ns) {
+        raise_timeout(c, p);
+        stop = 1;
+      }
+    }
+    if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+  }
+}
+
+// Wait used while tearing down: ignores the abort flag, still bounded.
+__device__ void wait_drain(uint32_t bar, uint32_t parity, const GemmParams& p) {
+  uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > p.timeout_ns) {
+      atomicOr(p.status, kStatusTimeout);
+      return;
+    }
+  }
+}
+
+// ---- striped partition --------------------------------------------------------
+
+// First unit of CTA c's stripe: floor(c * U / G).
+__device__ __forceinline__ long long stripe_begin(long long c, long long U, long long G) {
+  return (c * U) / G;
+}
+
+// CTA whose stripe holds unit u (every stripe is non-empty because G <= U).
+__device__ __forceinline__ long long stripe_owner(long long u, long long U, long long G) {
+  return ((u + 1) * G - 1) / U;
+}
+
+// ---- dequantisation -------------------------------------------------------------
+
+__device__ __forceinline__ __half2 as_h2(uint32_t v) {
+  return *reinterpret_cast<__half2*>(&v);
+}
+__device__ __forceinline__ uint32_t as_u32(__half2 v) {
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// One 32-bit word of 8 codes -> 4 fp16 pairs (k, k+1), (k+2, k+3), ... scaled.
+// Nibble positions 0..3 hold k offsets 0, 2, 4, 6 and positions 4..7 hold
+// 1, 3, 5, 7, so a 0x000F000F mask pulls a consecutive pair into the low 4 bits
+// of each half.  0x6400 | c is 1024 + c exactly (binary16 ulp is 1 on
+// [1024, 2048)); 0x6400 | (c << 4) is 1024 + 16c.  Subtracting 1024 + z (or
+// scaling by 1/16 and adding -(64 + z)) gives q - z exactly; the single
+// rounding of the whole dequantisation is the final multiply by the scale.
+__device__ __forceinline__ void dequant_word(uint32_t w, __half2 sub_lo, __half2 add_hi,
+                                             __half2 s2, uint32_t* out) {
+  const __half2 sixteenth = as_h2(0x2C002C00u);
+  const uint32_t w8 = w >> 8;
+  const uint32_t a = (w & 0x000F000Fu) | 0x64006400u;
+  const uint32_t b = (w & 0x00F000F0u) | 0x64006400u;
+  const uint32_t c = (w8 & 0x000F000Fu) | 0x64006400u;
+  const uint32_t d = (w8 & 0x00F000F0u) | 0x64006400u;
+  out[0] = as_u32(__hmul2(__hsub2(as_h2(a), sub_lo), s2));
+  out[1] = as_u32(__hmul2(__hfma2(as_h2(b), sixteenth, add_hi), s2));
+  out[2] = as_u32(__hmul2(__hsub2(as_h2(c), sub_lo), s2));
+  out[3] = as_u32(__hmul2(__hfma2(as_h2(d), sixteenth, add_hi), s2));
+}
+
+// ---- the kernel -----------------------------------------------------------------
+
+__global__ void __launch_bounds__(kThreads, 1)
+    w4a16_gemm_kernel(const __grid_constant__ CUtensorMap x_map, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment for the 128-byte-swizzled X tiles.
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
+  uint8_t* base = smem_raw + (base_addr - raw_addr);
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(base);
+  const uint32_t stage0 = base_addr + kCtrlBytes;
+  uint8_t* stage0_ptr = base + kCtrlBytes;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long U = p.units;
+  const long long G = gridDim.x;
+  const long long u_begin = stripe_begin(blockIdx.x, U, G);
+  const long long u_end = stripe_begin(blockIdx.x + 1, U, G);
+  const int S = p.stages;
+  const int cpu = p.cpu;
+
+  auto bar = [&](const uint64_t& b) { return smem_addr(&b); };
+
+  // ---- setup --------------------------------------------------------------------
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar(ctrl->full[s]), 1);
+      mbar_init(bar(ctrl->empty[s]), 4 * cpu + 1);
+    }
+    for (int a = 0; a < kAStages; ++a) {
+      mbar_init(bar(ctrl->afull[a]), 4);
+      mbar_init(bar(ctrl->aempty[a]), 1);
+    }
+    mbar_init(bar(ctrl->dfull), 1);
+    mbar_init(bar(ctrl->dempty), kNumDqWarps);
+    mbar_init(bar(ctrl->drain), 1);
+    mbar_init(bar(ctrl->red_arrive), kNumDqWarps);
+    mbar_init(bar(ctrl->red_go), 1);
+    ctrl->abort = 0;
+    ctrl->reduce_last = 0;
+    fence_mbarrier_init();
+    prefetch_tensormap(&x_map);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_addr(&ctrl->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctrl->tmem_base;
+
+  if (warp == 0) {
+    // ================= producer: TMA into the stage ring =================
+    if (lane == 0) {
+      const uint64_t pol_w = p.weights_reused ? policy_evict_last() : policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      const uint8_t* codes = reinterpret_cast<const uint8_t*>(p.codes);
+      const int KB = p.K / kChunkK;
+      long long issued = 0;
+      for (long long u = u_begin; u < u_end; ++u, ++issued) {
+        const int s = (int)(issued % S);
+        const uint32_t ph = (uint32_t)((issued / S) & 1);
+        if (!wait_thread(bar(ctrl->empty[s]), ph ^ 1u, ctrl, p)) break;
+        const long long tile = u / p.kt;
+        const int ku = (int)(u - tile * p.kt);
+        const int mt = (int)(tile / p.n_tiles);
+        const int nt = (int)(tile - (long long)mt * p.n_tiles);
+        const int k0 = ku * cpu * kChunkK;
+        const int g = k0 / p.group;
+        const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
+        const uint32_t fb = bar(ctrl->full[s]);
+        mbar_arrive_expect_tx(fb, p.tx_bytes);
+        bulk_g2s(st + p.off_codes,
+                 codes + ((size_t)nt * KB + (size_t)ku * cpu) * kChunkCodeBytes,
+                 (uint32_t)(cpu * kChunkCodeBytes), fb, pol_w);
+        bulk_g2s(st + p.off_scales, p.scales + (size_t)g * p.N + (size_t)nt * kTileN,
+                 kTileN * 2, fb, pol_w);
+        if (p.zeros)
+          bulk_g2s(st + p.off_zeros, p.zeros + (size_t)g * (p.N / 2) + (size_t)nt * (kTileN / 2),
+                   kTileN / 2, fb, pol_w);
+        for (int j = 0; j < cpu; ++j)
+          tma_load_2d(st + (uint32_t)j * p.x_chunk_bytes, &x_map, k0 + j * kChunkK, mt * p.bn, fb,
+                      pol_x);
+      }
+      // Wait for every copy still in flight before the CTA may exit.
+      const long long first = issued > S ? issued - S : 0;
+      for (long long i = first; i < issued; ++i)
+        wait_drain(bar(ctrl->full[i % S]), (uint32_t)((i / S) & 1), p);
+    }
+  } else if (warp == 1) {
+    // ================= MMA issuer (one thread) =================
+    if (lane == 0) {
+      const uint32_t idesc = umma_idesc_f16_f32((uint32_t)p.bn);
+      long long it = 0, ch = 0, seg = 0;
+      long long u = u_begin;
+      bool ok = true;
+      while (ok && u < u_end) {
+        const long long tile = u / p.kt;
+        const long long seg_end = min(u_end, (tile + 1) * p.kt);
+        if (seg > 0) {
+          if (!wait_thread(bar(ctrl->dempty), (uint32_t)((seg - 1) & 1), ctrl, p)) break;
+          tc_fence_after();
+        }
+        bool first = true;
+        for (; u < seg_end; ++u, ++it) {
+          const int s = (int)(it % S);
+          if (!wait_thread(bar(ctrl->full[s]), (uint32_t)((it / S) & 1), ctrl, p)) { ok = false; break; }
+          const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
+          for (int j = 0; j < cpu; ++j, ++ch) {
+            const int a = (int)(ch % kAStages);
+            if (!wait_thread(bar(ctrl->afull[a]), (uint32_t)((ch / kAStages) & 1), ctrl, p)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t xs = st + (uint32_t)j * p.x_chunk_bytes;
+            const uint32_t a_col = tmem + kAColBase + (uint32_t)a * (kChunkK / 2);
+#pragma unroll
+            for (int kk = 0; kk < kChunkK / 16; ++kk) {
+              mma_f16_ts(tmem, a_col + (uint32_t)kk * 8, umma_desc_sw128(xs + (uint32_t)kk * 32),
+                         idesc, first ? 0u : 1u);
+              first = false;
+            }
+            mma_commit(bar(ctrl->aempty[a]));
+          }
+          if (!ok) break;
+          mma_commit(bar(ctrl->empty[s]));
+        }
+        if (!ok) break;
+        mma_commit(bar(ctrl->dfull));
+        ++seg;
+      }
+      // Every issued MMA must finish before TMEM is released.
+      mma_commit(bar(ctrl->drain));
+      wait_drain(bar(ctrl->drain), 0, p);
+    }
+  } else if (warp >= kFirstDqWarp) {
+    // ================= dequantisation + epilogue (8 warps) =================
+    const int dq = warp - kFirstDqWarp;       // 0..7
+    const int wg = dq >> 2;                   // warpgroup: even / odd chunks
+    const int quarter = warp & 3;             // TMEM lane quarter this warp may touch
+    const int row = quarter * 32 + lane;      // output column within the tile
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const bool has_zeros = p.zeros != nullptr;
+    long long it = 0, ch = 0, seg = 0, npartial = 0;
+    long long u = u_begin;
+    const long long first_tile = u_begin / p.kt;
+    bool ok = true;
+    while (ok && u < u_end) {
+      const long long tile = u / p.kt;
+      const long long seg_begin = u;
+      const long long seg_end = min(u_end, (tile + 1) * p.kt);
+      const int mt = (int)(tile / p.n_tiles);
+      const int nt = (int)(tile - (long long)mt * p.n_tiles);
+      // ---- mainloop: dequantise this warpgroup's chunks into TMEM ----
+      for (; u < seg_end; ++u, ++it) {
+        const int s = (int)(it % S);
+        const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
+        const uint8_t* st_ptr = stage0_ptr + (size_t)s * p.stage_bytes;
+        for (int j = 0; j < cpu; ++j, ++ch) {
+          if ((int)(ch & 1) != wg) continue;
+          if (!wait_warp(bar(ctrl->full[s]), (uint32_t)((it / S) & 1), ctrl, p)) { ok = false; break; }
+          const uint32_t cw = st + p.off_codes + (uint32_t)j * kChunkCodeBytes + (uint32_t)row * 16;
+          const uint4 lo = lds128(cw);
+          const uint4 hi = lds128(cw + 2048);
+          const uint16_t s_bits = reinterpret_cast<const uint16_t*>(st_ptr + p.off_scales)[row];
+          uint32_t z = 8;
+          if (has_zeros) z = (st_ptr[p.off_zeros + (row >> 1)] >> ((row & 1) * 4)) & 0xFu;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(ctrl->empty[s]));
+
+          const uint32_t s2u = (uint32_t)s_bits | ((uint32_t)s_bits << 16);
+          const uint32_t sub_u = 0x6400u | z;
+          const uint32_t add_u = 0xD400u | (z << 4);
+          const __half2 s2 = as_h2(s2u);
+          const __half2 sub_lo = as_h2(sub_u | (sub_u << 16));
+          const __half2 add_hi = as_h2(add_u | (add_u << 16));
+          uint32_t v[32];
+          dequant_word(lo.x, sub_lo, add_hi, s2, v + 0);
+          dequant_word(lo.y, sub_lo, add_hi, s2, v + 4);
+          dequant_word(lo.z, sub_lo, add_hi, s2, v + 8);
+          dequant_word(lo.w, sub_lo, add_hi, s2, v + 12);
+          dequant_word(hi.x, sub_lo, add_hi, s2, v + 16);
+          dequant_word(hi.y, sub_lo, add_hi, s2, v + 20);
+          dequant_word(hi.z, sub_lo, add_hi, s2, v + 24);
+          dequant_word(hi.w, sub_lo, add_hi, s2, v + 28);
+
+          const int a = (int)(ch % kAStages);
+          if (!wait_warp(bar(ctrl->aempty[a]), (uint32_t)(((ch / kAStages) & 1) ^ 1), ctrl, p)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          tmem_st_x32(tmem + lane_off + kAColBase + (uint32_t)a * (kChunkK / 2), v);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(ctrl->afull[a]));
+        }
+        if (!ok) break;
+      }
+      if (!ok) break;
+
+      // ---- epilogue: accumulators -> fp16 Y, or fp32 partial tile ----
+      if (!wait_warp(bar(ctrl->dfull), (uint32_t)(seg & 1), ctrl, p)) break;
+      tc_fence_after();
+      const int kt_lo = (int)(seg_begin - tile * p.kt);
+      const int kt_hi = (int)(seg_end - tile * p.kt);
+      const bool whole = (kt_lo == 0 && kt_hi == p.kt);
+      const int slot = (tile == first_tile) ? 0 : 1;
+      float* part = p.partials + ((size_t)blockIdx.x * 2 + slot) * ((size_t)p.bn * kTileN);
+      const int m_base = mt * p.bn;
+      const size_t y_col = (size_t)nt * kTileN + row;
+      for (int cc = wg; cc < p.bn / 8; cc += 2) {
+        uint32_t r[8];
+        tmem_ld_x8(tmem + lane_off + (uint32_t)cc * 8, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int m = cc * 8 + c;
+          const float f = __uint_as_float(r[c]);
+          if (whole) {
+            if (m_base + m < p.M)
+              p.Y[(size_t)(m_base + m) * p.N + y_col] = __half_as_ushort(__float2half_rn(f));
+          } else {
+            part[(size_t)m * kTileN + row] = f;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(ctrl->dempty));
+
+      if (!whole) {
+        // ---- global reduction: the last CTA to store its partial sums the tile ----
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(ctrl->red_arrive));
+        const uint32_t rph = (uint32_t)(npartial & 1);
+        if (dq == 0) {
+          if (!wait_warp(bar(ctrl->red_arrive), rph, ctrl, p)) break;
+          if (lane == 0) {
+            const long long c_first = stripe_owner(tile * p.kt, U, G);
+            const long long c_last = stripe_owner(tile * p.kt + p.kt - 1, U, G);
+            const int expected = (int)(c_last - c_first + 1);
+            const int prev = atomicAdd(&p.counters[tile], 1);
+            const int last = (prev == expected - 1);
+            if (last) {
+              __threadfence();
+              p.counters[tile] = 0;  // leave the workspace zeroed for the next call
+            }
+            ctrl->reduce_last = last;
+            mbar_arrive(bar(ctrl->red_go));
+          }
+          __syncwarp();
+        }
+        if (!wait_warp(bar(ctrl->red_go), rph, ctrl, p)) break;
+        ++npartial;
+        if (*reinterpret_cast<volatile int*>(&ctrl->reduce_last)) {
+          __threadfence();
+          const long long c_first = stripe_owner(tile * p.kt, U, G);
+          const long long c_last = stripe_owner(tile * p.kt + p.kt - 1, U, G);
+          for (int cc = wg; cc < p.bn / 8; cc += 2) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const int m = cc * 8 + c;
+              if (m_base + m >= p.M) continue;
+              float acc = 0.f;
+              for (long long q = c_first; q <= c_last; ++q) {
+                const int qslot = (tile == stripe_begin(q, U, G) / p.kt) ? 0 : 1;
+                const float* qp = p.partials + ((size_t)q * 2 + qslot) * ((size_t)p.bn * kTileN);
+                acc += __ldcg(qp + (size_t)m * kTileN + row);
+              }
+              p.Y[(size_t)(m_base + m) * p.N + y_col] = __half_as_ushort(__float2half_rn(acc));
+            }
+          }
+        }
+      }
+      ++seg;
+    }
+  }
+
+  // ---- teardown -------------------------------------------------------------------
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t gemm_set_smem_limit(int bytes) {
+  return cudaFuncSetAttribute(w4a16_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+cudaError_t launch_gemm(const CUtensorMap& x_map, const GemmParams& p, int grid, uint32_t smem_bytes,
+                        cudaStream_t stream) {
+  w4a16_gemm_kernel<<<grid, kThreads, smem_bytes, stream>>>(x_map, p);
+  return cudaGetLastError();
+}
+
+}  // namespace w4a16

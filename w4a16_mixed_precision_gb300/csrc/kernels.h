@@ -1,0 +1,64 @@
+// kernels.h -- internal interface between the C-ABI host layer (api.cu) and
+// the device kernels (gemm.cu, repack.cu).  Not installed, not part of the ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace w4a16 {
+
+// Fixed geometry of the fused kernel.
+constexpr int kThreads = 384;      // 12 warps: producer, MMA, TMEM owner, spare, 8 dequant
+constexpr int kTileN = 128;        // output columns per tile = UMMA M
+constexpr int kChunkK = 64;        // K elements per dequantised A chunk
+constexpr int kChunkCodeBytes = kTileN * kChunkK / 2;  // 4096
+constexpr int kAStages = 8;        // A chunks resident in TMEM
+constexpr int kTmemCols = 512;
+constexpr int kAColBase = 256;     // TMEM column of A stage 0; D lives in columns [0, 256)
+constexpr int kMaxStages = 16;
+constexpr int kCtrlBytes = 1024;   // barriers and flags at the front of dynamic smem
+constexpr int kMaxBn = 256;        // tokens per m-tile (UMMA N)
+
+// Device status word bits (workspace offset 0).
+constexpr int kStatusTimeout = 1;
+
+struct GemmParams {
+  const uint32_t* codes;    // tile-layout codes
+  const uint16_t* scales;   // fp16 [G][N]
+  const uint8_t* zeros;     // packed zeros [G][N/2 bytes] or nullptr
+  uint16_t* Y;              // fp16 [M][N]
+  float* partials;          // [grid][2][bn][128] fp32
+  int* counters;            // [m_tiles * n_tiles]
+  int* status;              // status word
+  int M, K, N, group;
+  int bn;                   // tokens per m-tile, multiple of 16
+  int m_tiles, n_tiles;
+  int kt;                   // units per tile along K
+  int cpu;                  // 64-wide chunks per unit (1 or 2)
+  long long units;          // m_tiles * n_tiles * kt
+  int stages;
+  uint32_t stage_bytes;
+  uint32_t x_chunk_bytes;   // bn * 128
+  uint32_t off_codes, off_scales, off_zeros;  // byte offsets inside a stage
+  uint32_t tx_bytes;        // bytes landed per stage
+  int weights_reused;       // more than one m-tile reads the same weights
+  unsigned long long timeout_ns;
+};
+
+// Partition and resource plan of one marlin_gemm call.
+struct GemmPlan {
+  int bn, m_tiles, n_tiles, kt, cpu, stages, grid;
+  long long units;
+  uint32_t stage_bytes, smem_bytes;
+  size_t ws_counters_off, ws_partials_off, ws_bytes;
+};
+
+cudaError_t launch_gemm(const CUtensorMap& x_map, const GemmParams& p, int grid, uint32_t smem_bytes,
+                        cudaStream_t stream);
+cudaError_t gemm_set_smem_limit(int bytes);
+
+cudaError_t launch_repack(const uint32_t* q, uint32_t* out, int K, int N, cudaStream_t stream);
+cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, cudaStream_t stream);
+
+}  // namespace w4a16
