@@ -1,0 +1,546 @@
+"""Benchmark of the W4A16 fused matrix multiply on GB300.
+
+Default workload: the Llama-2-7B decode linears, symmetric group 128:
+(K, N) in {4096x12288 QKV, 4096x4096 O, 4096x22016 gate+up, 11008x4096 down},
+M in {1, 2, 4, 8, 16, 32}.  One step = the 24 matrix multiplies of that grid,
+each reading its weights from HBM: every call of a step reads its own copy
+of the layer's repacked weights (624 MB in all, more than two L2s), so no call
+finds its weights in L2.  The step is captured once as a CUDA graph and
+replayed.
+
+Output: one JSON line (rank 0).  value = algorithmic bytes of the whole step
+(codes + scales + X + Y) / step time, in GB/s, summed over ranks.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+--impl reference times the CPU oracle (the plain fp64 definition) on a bounded
+sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import ALL_CONFIGS, Problem, make_activations, make_weights, seed_for  # noqa: E402
+
+METRIC = "W4A16 GEMM µs, HBM GB/s & TFLOP/s (% roofline) vs M; speedup over FP16 GEMM"
+WORKLOAD_NAMES = {
+    "7b-decode": "llama2-7b-decode-linears (K,N) in {4096x12288, 4096x4096, 4096x22016, 11008x4096}, "
+                 "M in {1,2,4,8,16,32}, group 128, z=8",
+    "single": "single GEMM M=16 K=4096 N=4096 group 128 z=8",
+    "70b-decode": "llama2-70b batched decode (K,N) in {8192x10240, 8192x8192, 8192x57344, 28672x8192}, "
+                  "M in {1,4,16,32,64,128}, group 128, z=8",
+    "prefill": "prefill M in {1024,4096,8192} x (K,N) in {8192x8192, 8192x28672}, group 128, z=8",
+    "asym-odd": "asymmetric zeros, group 128 and per-column, (K,N) in {2048x2048, 2048x5632, 5120x15360, "
+                "13824x5120}, M in {1,16,48}",
+}
+L2_BYTES = 126 * 1024 * 1024
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "w4a16_mixed_precision_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """dram bytes per launch from a committed ncu capture, if the kernel sources
+    have not changed since it was taken; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_src") != kernel_source_digest():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ---- clocks --------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ["uuid", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, uuid: str | None):
+        self.uuid = (uuid or "").lower().replace("gpu-", "")
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            if self.uuid and self.uuid not in parts[0].lower():
+                continue
+            self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        inside = [s for (t, s) in self.samples if t0 <= t <= t1]
+        used = inside if inside else [s for (_, s) in self.samples]
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(s[1]) for s in used if num(s[1]) is not None]
+        smax = [num(s[2]) for s in used if num(s[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in used for i in range(4) if s[4 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(used), "samples_in_timed_region": len(inside)}
+
+
+# ---- distributed ------------------------------------------------------------------
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, world, local
+
+
+def dist_max(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---- CPU oracle baseline ------------------------------------------------------------
+
+class OracleSampler:
+    """Times the CPU oracle (as it stands) on column samples of the workload.
+
+    A sample of problem p = all M rows x `cols` random columns; its share of
+    the algorithmic bytes is p.algorithmic_bytes() * cols / N."""
+
+    def __init__(self, threads: int):
+        import oracle
+        oracle.build()
+        self.oracle = oracle
+        self.threads = threads
+        self.cache = {}
+        self.sec_per_mk = None
+
+    def inputs(self, p):
+        if p.key not in self.cache:
+            Qp, S, Zp = make_weights(p.K, p.N, p.group, p.asym, seed_for(p.key))
+            X = make_activations(p.M, p.K, seed_for(p.key) + 1)
+            self.cache = {p.key: (X, Qp, S, Zp)}   # keep one problem's inputs at a time
+        return self.cache[p.key]
+
+    def calibrate(self, p):
+        X, Qp, S, Zp = self.inputs(p)
+        t = time.perf_counter()
+        self.oracle.w4a16(X, Qp, S, Zp, p.group, p.N, idx=np.arange(p.M) * p.N, threads=1)
+        self.sec_per_mk = max((time.perf_counter() - t) / (p.M * p.K), 1e-10)
+
+    def run(self, p, budget_s: float):
+        """Returns (bytes credited, seconds, columns)."""
+        if self.sec_per_mk is None:
+            self.calibrate(p)
+        X, Qp, S, Zp = self.inputs(p)
+        cols = int(budget_s * self.threads / (self.sec_per_mk * p.M * p.K))
+        cols = max(1, min(p.N, cols))
+        rng = np.random.default_rng(seed_for(p.key))
+        sel = np.sort(rng.choice(p.N, cols, replace=False))
+        idx = (np.arange(p.M)[:, None] * p.N + sel[None, :]).ravel()
+        t = time.perf_counter()
+        self.oracle.w4a16(X, Qp, S, Zp, p.group, p.N, idx=idx, threads=self.threads)
+        dt = time.perf_counter() - t
+        return p.algorithmic_bytes() * cols / p.N, dt, cols
+
+
+def oracle_baseline(problems, budget_s: float, threads: int):
+    """(GB/s, seconds, sample description) over every problem of the workload."""
+    smp = OracleSampler(threads)
+    tot_b = tot_s = 0.0
+    cols = []
+    for p in problems:
+        b, s, c = smp.run(p, budget_s / len(problems))
+        tot_b += b
+        tot_s += s
+        cols.append(c)
+    desc = (f"all {len(problems)} problems of the workload, each: all M rows x {min(cols)}-{max(cols)} "
+            f"random columns (of N); bytes credited = algorithmic bytes x sampled columns / N")
+    return tot_b / tot_s / 1e9, tot_s, desc
+
+
+def run_reference(args, problems, rank, world):
+    if rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    smp = OracleSampler(threads)
+    steps = args.steps + args.warmup
+    budget = max(0.02, min(10.0, 90.0 / max(steps, 1)))
+    # one step = one problem of the workload (cycling), a column sample sized to the budget;
+    # steps walk the problems in order so consecutive steps reuse inputs
+    order = sorted(range(len(problems)), key=lambda i: problems[i].key)
+    tot_b = tot_s = 0.0
+    cols = []
+    for i in range(steps):
+        p = problems[order[(i * len(problems)) // steps if steps >= len(problems) else i % len(problems)]]
+        b, s, c = smp.run(p, budget)
+        if i >= args.warmup:
+            tot_b += b
+            tot_s += s
+            cols.append(c)
+    value = tot_b / tot_s / 1e9
+    desc = (f"each step: one problem of the workload (steps walk all {len(problems)}), all M rows x "
+            f"{min(cols)}-{max(cols)} random columns; bytes credited = algorithmic bytes x columns / N")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_s / max(args.steps, 1) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD_NAMES[args.workload]},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---- GPU arm -------------------------------------------------------------------------
+
+def run_gpu(args, problems, rank, world, local):
+    import torch
+
+    import w4a16_mixed_precision_gb300 as w4
+    from w4a16_mixed_precision_gb300 import build as cuda_build
+
+    cuda_build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = load_peaks()
+
+    # ---- weights: rotating copies so that no call finds its weights in L2 ----
+    # Each layer gets uses_per_step * P copies and every copy is read once per P
+    # steps, P chosen so that P steps stream more than two L2s of weights.
+    layers = sorted({(p.K, p.N, p.group, p.asym) for p in problems})
+
+    def wbytes(K, N, g, a):
+        return K * N // 2 + (K // g) * N * 2 + ((K // g) * N // 2 if a else 0)
+
+    uses = {lk: sum(1 for p in problems if (p.K, p.N, p.group, p.asym) == lk) for lk in layers}
+    step_wbytes = sum(wbytes(*lk) * uses[lk] for lk in layers)
+    P = max(1, -(-2 * L2_BYTES // step_wbytes))
+    packed = {}
+    for (K, N, g, a) in layers:
+        Qp, S, Zp = make_weights(K, N, g, a, seed=seed_for(f"w:{K}:{N}:{g}:{int(a)}"))
+        pw = w4.repack(torch.from_numpy(Qp).to(dev), torch.from_numpy(S).to(dev),
+                       torch.from_numpy(Zp).to(dev) if a else None, g)
+        copies = [pw]
+        # the graphs use uses*P copies; the per-run table rotates through enough
+        # copies of this one layer to stream more than two L2s between reuses
+        n_copies = max(uses[(K, N, g, a)] * P, -(-2 * L2_BYTES // wbytes(K, N, g, a)) + 1)
+        for _ in range(n_copies - 1):
+            copies.append(w4.PackedWeights(pw.buf.clone(), pw.K, pw.N, pw.group, pw.has_zeros,
+                                           pw.off_scales, pw.off_zeros))
+        packed[(K, N, g, a)] = copies
+    weight_copies_bytes = sum(wbytes(*lk) * len(packed[lk]) for lk in layers)
+    max_m = max(p.M for p in problems)
+    ws = {lk: w4.Workspace(max_m, lk[0], lk[1], lk[2]) for lk in layers}
+    xs = [torch.from_numpy(make_activations(p.M, p.K, seed_for(p.key))).to(dev) for p in problems]
+    ys = [torch.empty((p.M, p.N), dtype=torch.float16, device=dev) for p in problems]
+    plans = []  # per phase: (problem index, weight copy) in step order
+    for c in range(P):
+        seen = {lk: 0 for lk in layers}
+        plan = []
+        for i, p in enumerate(problems):
+            lk = (p.K, p.N, p.group, p.asym)
+            plan.append((i, c * uses[lk] + seen[lk]))
+            seen[lk] += 1
+        plans.append(plan)
+
+    def step(plan):
+        for i, c in plan:
+            p = problems[i]
+            lk = (p.K, p.N, p.group, p.asym)
+            w4.gemm_into(xs[i], packed[lk][c], ws[lk], ys[i])
+
+    # eager warm-up (one-time host set-up happens outside the graphs)
+    for plan in plans:
+        step(plan)
+    torch.cuda.synchronize()
+    for lk in layers:
+        assert w4.device_status(ws[lk]) == 0
+
+    stream = torch.cuda.Stream()
+    graphs = []
+    with torch.cuda.stream(stream):
+        for plan in plans:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(plan)
+            graphs.append(g)
+    torch.cuda.synchronize()
+
+    step_bytes = sum(p.algorithmic_bytes() for p in problems)
+    step_flops = sum(p.flops() for p in problems)
+
+    props = torch.cuda.get_device_properties(dev)
+    sampler = ClockSampler(str(getattr(props, "uuid", "")))
+    sampler.start()
+    # clock soak: keep the GPU busy ~1 s before the timed region
+    with torch.cuda.stream(stream):
+        t_end = time.time() + (0.0 if args.no_soak else 1.0)
+        while time.time() < t_end:
+            for i in range(20):
+                graphs[i % P].replay()
+            stream.synchronize()
+        for i in range(args.warmup):
+            graphs[i % P].replay()
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(args.steps):
+            graphs[i % P].replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    time.sleep(0.25)
+    sampler.stop()
+    ms_total = ev0.elapsed_time(ev1)
+    ms_total = dist_max(ms_total, world)
+    ms_per_step = ms_total / args.steps
+    for lk in layers:
+        assert w4.device_status(ws[lk]) == 0, "a kernel reported an expired wait"
+
+    value = step_bytes * world / (ms_per_step * 1e-3) / 1e9
+    launches = len(problems)
+    achieved = step_bytes / (ms_per_step * 1e-3) / 1e9
+    clocks = sampler.summary(t_wall0 - 1.2, t_wall1)
+
+    # ---- per-run table (outside the timed region): our kernel vs cuBLAS fp16 ----
+    runs = []
+    if not args.no_table:
+        runs = per_run_table(problems, packed, ws, xs, ys, dev, peaks)
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None if args.no_e2e else end_to_end(problems, packed, ws, plans, dev, args, step_bytes)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAMES[args.workload],
+                   "problems_per_step": launches, "graph_phases": P,
+                   "l2": f"inputs larger than L2: rotating weight copies ({weight_copies_bytes / 1e6:.0f} MB "
+                         f"in all), each read once per {P} step(s), so no call finds its weights in L2",
+                   "timing": "step captured as a CUDA graph (one per rotation phase), replayed K times; "
+                             "CUDA events on the replay stream",
+                   "step_bytes": step_bytes, "step_flops": step_flops},
+        "gpu_launches": launches * args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(args.workload),
+                     "peak_source": peaks["source"],
+                     "kernel": "w4a16_gemm_kernel (every launch of the step)",
+                     "bytes_per_launch": step_bytes / launches,
+                     "avg_launch_us": ms_per_step * 1e3 / launches},
+        "clocks": clocks,
+        "e2e": e2e,
+        "runs": runs,
+    }
+    if args.workload == "prefill":
+        tf = step_flops / (ms_per_step * 1e-3) / 1e12
+        line["roofline"] = {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
+                            "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"], "traffic": None,
+                            "peak_source": peaks["source"] + " bf16 (fp16 dense rate is the same)",
+                            "kernel": "w4a16_gemm_kernel"}
+    if rank == 0 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        v, s, desc = oracle_baseline(problems, args.cpu_budget, threads)
+        line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                "sample": desc, "seconds": s}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def per_run_table(problems, packed, ws, xs, ys, dev, peaks, reps=60):
+    import torch
+
+    import w4a16_mixed_precision_gb300 as w4
+    out = []
+    fp16_w = {}
+    for p in problems:
+        lk = (p.K, p.N, p.group, p.asym)
+        if lk not in fp16_w:
+            g = torch.Generator(device=dev)
+            g.manual_seed(p.K * 31 + p.N)
+            # enough fp16 copies that a rotation streams more than two L2s
+            n = max(2, min(len(packed[lk]), -(-2 * L2_BYTES // (p.K * p.N * 2)) + 1))
+            fp16_w[lk] = [torch.randn((p.K, p.N), dtype=torch.float16, device=dev, generator=g)
+                          for _ in range(n)]
+    for i, p in enumerate(problems):
+        lk = (p.K, p.N, p.group, p.asym)
+        R = len(packed[lk])
+        Rf = len(fp16_w[lk])
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(3):
+            w4.gemm_into(xs[i], packed[lk][0], ws[lk], ys[i])
+        torch.cuda.synchronize()
+        s0.record()
+        for r in range(reps):
+            w4.gemm_into(xs[i], packed[lk][r % R], ws[lk], ys[i])
+        s1.record()
+        torch.cuda.synchronize()
+        us = s0.elapsed_time(s1) * 1e3 / reps
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(3):
+            torch.matmul(xs[i], fp16_w[lk][0])
+        torch.cuda.synchronize()
+        c0.record()
+        for r in range(reps):
+            torch.matmul(xs[i], fp16_w[lk][r % Rf])
+        c1.record()
+        torch.cuda.synchronize()
+        cu = c0.elapsed_time(c1) * 1e3 / reps
+        gbs = p.algorithmic_bytes() / (us * 1e-6) / 1e9
+        tfl = p.flops() / (us * 1e-6) / 1e12
+        out.append({"M": p.M, "K": p.K, "N": p.N, "group": p.group, "zeros": p.asym, "us": round(us, 3),
+                    "GBps": round(gbs, 1), "TFLOPs": round(tfl, 2),
+                    "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+                    "tensor_frac": round(tfl / peaks["bf16_tflops"], 4),
+                    "cublas_fp16_us": round(cu, 3), "speedup_vs_fp16": round(cu / us, 3)})
+    return out
+
+
+def end_to_end(problems, packed, ws, plans, dev, args, step_bytes):
+    import torch
+
+    import w4a16_mixed_precision_gb300 as w4
+    hx = [torch.from_numpy(make_activations(p.M, p.K, seed_for(p.key))).pin_memory() for p in problems]
+    hy = [torch.empty((p.M, p.N), dtype=torch.float16).pin_memory() for p in problems]
+    dx = [torch.empty((p.M, p.K), dtype=torch.float16, device=dev) for p in problems]
+    dy = [torch.empty((p.M, p.N), dtype=torch.float16, device=dev) for p in problems]
+    h2d = sum(t.numel() * 2 for t in hx)
+    d2h = sum(t.numel() * 2 for t in hy)
+    steps = max(3, min(args.steps, 200))
+
+    def one(plan):
+        for i, c in plan:
+            p = problems[i]
+            lk = (p.K, p.N, p.group, p.asym)
+            dx[i].copy_(hx[i], non_blocking=True)
+            w4.gemm_into(dx[i], packed[lk][c], ws[lk], dy[i])
+            hy[i].copy_(dy[i], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for k in range(3):
+        one(plans[k % len(plans)])
+    t0 = time.perf_counter()
+    for k in range(steps):
+        one(plans[k % len(plans)])
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": step_bytes / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3, "steps": steps,
+            "path": "marlin_gemm via the Python binding, pinned host X in, Y out, per call"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="7b-decode", choices=sorted(ALL_CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-table", action="store_true", help="skip the per-run table")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
+    ap.add_argument("--no-soak", action="store_true", help="skip the 1 s clock soak (profiling)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    problems = ALL_CONFIGS[args.workload]
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, problems, rank, int(os.environ.get("WORLD_SIZE", "1")))
+        return
+    rank, world, local = dist_setup(args.gpus)
+    run_gpu(args, problems, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
