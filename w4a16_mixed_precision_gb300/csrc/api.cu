@@ -175,7 +175,7 @@ marlin_status_t marlin_gemm(const uint16_t* X, const void* packed, const uint16_
   if ((s = get_encoder()) != MARLIN_OK) return s;
 
   const GemmPlan g = make_plan(M, K, N, d->sms, d->smem_optin, zeros != nullptr);
-  if (g.stages < 2) return MARLIN_ERR_UNSUPPORTED;
+  if (g.stages < 2 || g.units > 0x7FFFFFFFLL / 2) return MARLIN_ERR_UNSUPPORTED;
   if (workspace_bytes < g.ws_bytes) return MARLIN_ERR_WORKSPACE_TOO_SMALL;
 
   {

@@ -54,51 +54,46 @@ constexpr int kNumDqWarps = 8;
 constexpr int kFirstDqWarp = 4;
 
 // ---- bounded waits ----------------------------------------------------------
+// Each wait sleeps inside mbarrier.try_wait (woken when the phase completes)
+// and checks the abort flag and the global timer between sleeps.  The loops
+// are kept small and not unrolled: the kernel's roles run different code and
+// share one instruction cache.
 
-__device__ __forceinline__ void raise_timeout(Ctrl* c, const GemmParams& p) {
+__device__ __noinline__ void raise_timeout(Ctrl* c, const GemmParams& p) {
   *reinterpret_cast<volatile int*>(&c->abort) = 1;
   atomicOr(p.status, kStatusTimeout);
 }
 
-// Single-thread wait.  Returns false when the CTA is aborting or the wait expired.
-__device__ bool wait_thread(uint32_t bar, uint32_t parity, Ctrl* c, const GemmParams& p) {
-  if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = global_timer_ns();
-  while (true) {
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+// Slow path of a wait: returns false when the CTA is aborting or the wait expired.
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, Ctrl* c, const GemmParams& p) {
+  const uint64_t t0 = global_timer_ns();
+#pragma unroll 1
+  while (!mbar_try_wait(bar, parity)) {
     if (*reinterpret_cast<volatile int*>(&c->abort)) return false;
     if (global_timer_ns() - t0 > p.timeout_ns) {
       raise_timeout(c, p);
       return false;
     }
   }
+  return true;
+}
+
+__device__ __forceinline__ bool wait_thread(uint32_t bar, uint32_t parity, Ctrl* c,
+                                            const GemmParams& p) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, c, p);
 }
 
 // Whole-warp wait with a warp-uniform outcome.
-__device__ bool wait_warp(uint32_t bar, uint32_t parity, Ctrl* c, const GemmParams& p) {
-  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-  const uint32_t lane = threadIdx.x & 31;
-  uint64_t t0 = global_timer_ns();
-  while (true) {
-    for (int i = 0; i < 32; ++i)
-      if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-    int stop = 0;
-    if (lane == 0) {
-      if (*reinterpret_cast<volatile int*>(&c->abort)) {
-        stop = 1;
-      } else if (global_timer_ns() - t0 > p.timeout_ns) {
-        raise_timeout(c, p);
-        stop = 1;
-      }
-    }
-    if (__shfl_sync(0xffffffffu, stop, 0)) return false;
-  }
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, Ctrl* c,
+                                          const GemmParams& p) {
+  return __all_sync(0xffffffffu, wait_thread(bar, parity, c, p));
 }
 
 // Wait used while tearing down: ignores the abort flag, still bounded.
-__device__ void wait_drain(uint32_t bar, uint32_t parity, const GemmParams& p) {
-  uint64_t t0 = global_timer_ns();
+__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, const GemmParams& p) {
+  const uint64_t t0 = global_timer_ns();
+#pragma unroll 1
   while (!mbar_try_wait(bar, parity)) {
     if (global_timer_ns() - t0 > p.timeout_ns) {
       atomicOr(p.status, kStatusTimeout);
@@ -150,6 +145,10 @@ __device__ __forceinline__ void dequant_word(uint32_t w, __half2 sub_lo, __half2
 }
 
 // ---- the kernel -----------------------------------------------------------------
+//
+// Hot loops advance their ring positions and unit coordinates incrementally:
+// the producer and the MMA issuer are single threads, so any integer division
+// on their path sits directly on the critical path of the whole CTA.
 
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_gemm_kernel(const __grid_constant__ CUtensorMap x_map, const GemmParams p) {
@@ -160,16 +159,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* base = smem_raw + (base_addr - raw_addr);
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(base);
   const uint32_t stage0 = base_addr + kCtrlBytes;
-  uint8_t* stage0_ptr = base + kCtrlBytes;
+  const uint8_t* stage0_ptr = base + kCtrlBytes;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const long long U = p.units;
   const long long G = gridDim.x;
-  const long long u_begin = stripe_begin(blockIdx.x, U, G);
-  const long long u_end = stripe_begin(blockIdx.x + 1, U, G);
+  const int u_begin = (int)stripe_begin(blockIdx.x, U, G);
+  const int u_end = (int)stripe_begin(blockIdx.x + 1, U, G);
+  const int KT = p.kt;
   const int S = p.stages;
   const int cpu = p.cpu;
+  const int tile_begin = u_begin / KT;
+  const int ku_begin = u_begin - tile_begin * KT;
 
   auto bar = [&](const uint64_t& b) { return smem_addr(&b); };
 
@@ -209,79 +211,85 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_x = policy_evict_last();
       const uint8_t* codes = reinterpret_cast<const uint8_t*>(p.codes);
       const int KB = p.K / kChunkK;
-      long long issued = 0;
-      for (long long u = u_begin; u < u_end; ++u, ++issued) {
-        const int s = (int)(issued % S);
-        const uint32_t ph = (uint32_t)((issued / S) & 1);
+      const uint32_t code_bytes = (uint32_t)(cpu * kChunkCodeBytes);
+      const int units_per_group = p.group / (cpu * kChunkK);
+      int mt = tile_begin / p.n_tiles;
+      int nt = tile_begin - mt * p.n_tiles;
+      int ku = ku_begin;
+      int g = ku / units_per_group, ku_in_g = ku - g * units_per_group;
+      int s = 0;
+      uint32_t ph = 0;
+      int issued = 0;
+      for (int u = u_begin; u < u_end; ++u) {
         if (!wait_thread(bar(ctrl->empty[s]), ph ^ 1u, ctrl, p)) break;
-        const long long tile = u / p.kt;
-        const int ku = (int)(u - tile * p.kt);
-        const int mt = (int)(tile / p.n_tiles);
-        const int nt = (int)(tile - (long long)mt * p.n_tiles);
         const int k0 = ku * cpu * kChunkK;
-        const int g = k0 / p.group;
         const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
         const uint32_t fb = bar(ctrl->full[s]);
         mbar_arrive_expect_tx(fb, p.tx_bytes);
-        bulk_g2s(st + p.off_codes,
-                 codes + ((size_t)nt * KB + (size_t)ku * cpu) * kChunkCodeBytes,
-                 (uint32_t)(cpu * kChunkCodeBytes), fb, pol_w);
-        bulk_g2s(st + p.off_scales, p.scales + (size_t)g * p.N + (size_t)nt * kTileN,
-                 kTileN * 2, fb, pol_w);
+        bulk_g2s(st + p.off_codes, codes + ((size_t)nt * KB + (size_t)ku * cpu) * kChunkCodeBytes,
+                 code_bytes, fb, pol_w);
+        bulk_g2s(st + p.off_scales, p.scales + (size_t)g * p.N + (size_t)nt * kTileN, kTileN * 2, fb,
+                 pol_w);
         if (p.zeros)
           bulk_g2s(st + p.off_zeros, p.zeros + (size_t)g * (p.N / 2) + (size_t)nt * (kTileN / 2),
                    kTileN / 2, fb, pol_w);
         for (int j = 0; j < cpu; ++j)
           tma_load_2d(st + (uint32_t)j * p.x_chunk_bytes, &x_map, k0 + j * kChunkK, mt * p.bn, fb,
                       pol_x);
+        ++issued;
+        if (++s == S) { s = 0; ph ^= 1u; }
+        if (++ku_in_g == units_per_group) { ku_in_g = 0; ++g; }
+        if (++ku == KT) {
+          ku = 0; g = 0; ku_in_g = 0;
+          if (++nt == p.n_tiles) { nt = 0; ++mt; }
+        }
       }
       // Wait for every copy still in flight before the CTA may exit.
-      const long long first = issued > S ? issued - S : 0;
-      for (long long i = first; i < issued; ++i)
+      const int first = issued > S ? issued - S : 0;
+      for (int i = first; i < issued; ++i)
         wait_drain(bar(ctrl->full[i % S]), (uint32_t)((i / S) & 1), p);
     }
   } else if (warp == 1) {
     // ================= MMA issuer (one thread) =================
     if (lane == 0) {
       const uint32_t idesc = umma_idesc_f16_f32((uint32_t)p.bn);
-      long long it = 0, ch = 0, seg = 0;
-      long long u = u_begin;
+      int s = 0, a = 0, seg = 0;
+      uint32_t ph = 0, aph = 0;
+      int u = u_begin, ku = ku_begin;
       bool ok = true;
       while (ok && u < u_end) {
-        const long long tile = u / p.kt;
-        const long long seg_end = min(u_end, (tile + 1) * p.kt);
+        const int seg_len = min(u_end - u, KT - ku);
         if (seg > 0) {
           if (!wait_thread(bar(ctrl->dempty), (uint32_t)((seg - 1) & 1), ctrl, p)) break;
           tc_fence_after();
         }
-        bool first = true;
-        for (; u < seg_end; ++u, ++it) {
-          const int s = (int)(it % S);
-          if (!wait_thread(bar(ctrl->full[s]), (uint32_t)((it / S) & 1), ctrl, p)) { ok = false; break; }
+        uint32_t acc = 0;
+        for (int i = 0; i < seg_len && ok; ++i) {
+          if (!wait_thread(bar(ctrl->full[s]), ph, ctrl, p)) { ok = false; break; }
           const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
-          for (int j = 0; j < cpu; ++j, ++ch) {
-            const int a = (int)(ch % kAStages);
-            if (!wait_thread(bar(ctrl->afull[a]), (uint32_t)((ch / kAStages) & 1), ctrl, p)) {
-              ok = false;
-              break;
-            }
+          for (int j = 0; j < cpu; ++j) {
+            if (!wait_thread(bar(ctrl->afull[a]), aph, ctrl, p)) { ok = false; break; }
             tc_fence_after();
             const uint32_t xs = st + (uint32_t)j * p.x_chunk_bytes;
             const uint32_t a_col = tmem + kAColBase + (uint32_t)a * (kChunkK / 2);
 #pragma unroll
             for (int kk = 0; kk < kChunkK / 16; ++kk) {
               mma_f16_ts(tmem, a_col + (uint32_t)kk * 8, umma_desc_sw128(xs + (uint32_t)kk * 32),
-                         idesc, first ? 0u : 1u);
-              first = false;
+                         idesc, acc);
+              acc = 1;
             }
             mma_commit(bar(ctrl->aempty[a]));
+            if (++a == kAStages) { a = 0; aph ^= 1u; }
           }
           if (!ok) break;
           mma_commit(bar(ctrl->empty[s]));
+          if (++s == S) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
         mma_commit(bar(ctrl->dfull));
         ++seg;
+        u += seg_len;
+        ku = 0;
       }
       // Every issued MMA must finish before TMEM is released.
       mma_commit(bar(ctrl->drain));
@@ -295,72 +303,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = quarter * 32 + lane;      // output column within the tile
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const bool has_zeros = p.zeros != nullptr;
-    long long it = 0, ch = 0, seg = 0, npartial = 0;
-    long long u = u_begin;
-    const long long first_tile = u_begin / p.kt;
+    int s = 0, a = 0, ch = 0, seg = 0, npartial = 0;
+    uint32_t ph = 0, aph = 0;
+    int u = u_begin, ku = ku_begin, tile = tile_begin;
     bool ok = true;
     while (ok && u < u_end) {
-      const long long tile = u / p.kt;
-      const long long seg_begin = u;
-      const long long seg_end = min(u_end, (tile + 1) * p.kt);
-      const int mt = (int)(tile / p.n_tiles);
-      const int nt = (int)(tile - (long long)mt * p.n_tiles);
+      const int seg_len = min(u_end - u, KT - ku);
+      const int mt = tile / p.n_tiles;
+      const int nt = tile - mt * p.n_tiles;
       // ---- mainloop: dequantise this warpgroup's chunks into TMEM ----
-      for (; u < seg_end; ++u, ++it) {
-        const int s = (int)(it % S);
+      for (int i = 0; i < seg_len && ok; ++i) {
         const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
         const uint8_t* st_ptr = stage0_ptr + (size_t)s * p.stage_bytes;
-        for (int j = 0; j < cpu; ++j, ++ch) {
-          if ((int)(ch & 1) != wg) continue;
-          if (!wait_warp(bar(ctrl->full[s]), (uint32_t)((it / S) & 1), ctrl, p)) { ok = false; break; }
-          const uint32_t cw = st + p.off_codes + (uint32_t)j * kChunkCodeBytes + (uint32_t)row * 16;
-          const uint4 lo = lds128(cw);
-          const uint4 hi = lds128(cw + 2048);
-          const uint16_t s_bits = reinterpret_cast<const uint16_t*>(st_ptr + p.off_scales)[row];
-          uint32_t z = 8;
-          if (has_zeros) z = (st_ptr[p.off_zeros + (row >> 1)] >> ((row & 1) * 4)) & 0xFu;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(ctrl->empty[s]));
+        for (int j = 0; j < cpu; ++j) {
+          if ((ch & 1) == wg) {
+            if (!wait_warp(bar(ctrl->full[s]), ph, ctrl, p)) { ok = false; break; }
+            const uint32_t cw = st + p.off_codes + (uint32_t)j * kChunkCodeBytes + (uint32_t)row * 16;
+            const uint4 lo = lds128(cw);
+            const uint4 hi = lds128(cw + 2048);
+            const uint16_t s_bits = reinterpret_cast<const uint16_t*>(st_ptr + p.off_scales)[row];
+            uint32_t z = 8;
+            if (has_zeros) z = (st_ptr[p.off_zeros + (row >> 1)] >> ((row & 1) * 4)) & 0xFu;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(ctrl->empty[s]));
 
-          const uint32_t s2u = (uint32_t)s_bits | ((uint32_t)s_bits << 16);
-          const uint32_t sub_u = 0x6400u | z;
-          const uint32_t add_u = 0xD400u | (z << 4);
-          const __half2 s2 = as_h2(s2u);
-          const __half2 sub_lo = as_h2(sub_u | (sub_u << 16));
-          const __half2 add_hi = as_h2(add_u | (add_u << 16));
-          uint32_t v[32];
-          dequant_word(lo.x, sub_lo, add_hi, s2, v + 0);
-          dequant_word(lo.y, sub_lo, add_hi, s2, v + 4);
-          dequant_word(lo.z, sub_lo, add_hi, s2, v + 8);
-          dequant_word(lo.w, sub_lo, add_hi, s2, v + 12);
-          dequant_word(hi.x, sub_lo, add_hi, s2, v + 16);
-          dequant_word(hi.y, sub_lo, add_hi, s2, v + 20);
-          dequant_word(hi.z, sub_lo, add_hi, s2, v + 24);
-          dequant_word(hi.w, sub_lo, add_hi, s2, v + 28);
+            const uint32_t s2u = (uint32_t)s_bits | ((uint32_t)s_bits << 16);
+            const uint32_t sub_u = 0x6400u | z;
+            const uint32_t add_u = 0xD400u | (z << 4);
+            const __half2 s2 = as_h2(s2u);
+            const __half2 sub_lo = as_h2(sub_u | (sub_u << 16));
+            const __half2 add_hi = as_h2(add_u | (add_u << 16));
+            uint32_t v[32];
+            dequant_word(lo.x, sub_lo, add_hi, s2, v + 0);
+            dequant_word(lo.y, sub_lo, add_hi, s2, v + 4);
+            dequant_word(lo.z, sub_lo, add_hi, s2, v + 8);
+            dequant_word(lo.w, sub_lo, add_hi, s2, v + 12);
+            dequant_word(hi.x, sub_lo, add_hi, s2, v + 16);
+            dequant_word(hi.y, sub_lo, add_hi, s2, v + 20);
+            dequant_word(hi.z, sub_lo, add_hi, s2, v + 24);
+            dequant_word(hi.w, sub_lo, add_hi, s2, v + 28);
 
-          const int a = (int)(ch % kAStages);
-          if (!wait_warp(bar(ctrl->aempty[a]), (uint32_t)(((ch / kAStages) & 1) ^ 1), ctrl, p)) {
-            ok = false;
-            break;
+            if (!wait_warp(bar(ctrl->aempty[a]), aph ^ 1u, ctrl, p)) { ok = false; break; }
+            tc_fence_after();
+            tmem_st_x32(tmem + lane_off + kAColBase + (uint32_t)a * (kChunkK / 2), v);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(ctrl->afull[a]));
           }
-          tc_fence_after();
-          tmem_st_x32(tmem + lane_off + kAColBase + (uint32_t)a * (kChunkK / 2), v);
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(ctrl->afull[a]));
+          ++ch;
+          if (++a == kAStages) { a = 0; aph ^= 1u; }
         }
-        if (!ok) break;
+        if (++s == S) { s = 0; ph ^= 1u; }
       }
       if (!ok) break;
 
       // ---- epilogue: accumulators -> fp16 Y, or fp32 partial tile ----
       if (!wait_warp(bar(ctrl->dfull), (uint32_t)(seg & 1), ctrl, p)) break;
       tc_fence_after();
-      const int kt_lo = (int)(seg_begin - tile * p.kt);
-      const int kt_hi = (int)(seg_end - tile * p.kt);
-      const bool whole = (kt_lo == 0 && kt_hi == p.kt);
-      const int slot = (tile == first_tile) ? 0 : 1;
+      const bool whole = (ku == 0 && seg_len == KT);
+      const int slot = (tile == tile_begin) ? 0 : 1;
       float* part = p.partials + ((size_t)blockIdx.x * 2 + slot) * ((size_t)p.bn * kTileN);
       const int m_base = mt * p.bn;
       const size_t y_col = (size_t)nt * kTileN + row;
@@ -386,15 +388,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       if (!whole) {
         // ---- global reduction: the last CTA to store its partial sums the tile ----
-        __threadfence();
+        // The warps' partial stores are ordered before the leader's arrival
+        // count by the CTA-scoped mbarrier and the leader's gpu-scoped fence.
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(ctrl->red_arrive));
         const uint32_t rph = (uint32_t)(npartial & 1);
+        const long long c_first = stripe_owner((long long)tile * KT, U, G);
+        const long long c_last = stripe_owner((long long)tile * KT + KT - 1, U, G);
         if (dq == 0) {
           if (!wait_warp(bar(ctrl->red_arrive), rph, ctrl, p)) break;
           if (lane == 0) {
-            const long long c_first = stripe_owner(tile * p.kt, U, G);
-            const long long c_last = stripe_owner(tile * p.kt + p.kt - 1, U, G);
+            __threadfence();
             const int expected = (int)(c_last - c_first + 1);
             const int prev = atomicAdd(&p.counters[tile], 1);
             const int last = (prev == expected - 1);
@@ -410,30 +414,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_warp(bar(ctrl->red_go), rph, ctrl, p)) break;
         ++npartial;
         if (*reinterpret_cast<volatile int*>(&ctrl->reduce_last)) {
-          __threadfence();
-          const long long c_first = stripe_owner(tile * p.kt, U, G);
-          const long long c_last = stripe_owner(tile * p.kt + p.kt - 1, U, G);
+          // Sum the contributors' partial tiles in stripe order (fixed, so the
+          // result is bit-reproducible).  Loads of 4 contributors x 8 columns
+          // are issued together to overlap their L2 latency.
           for (int cc = wg; cc < p.bn / 8; cc += 2) {
+            float acc[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) acc[c] = 0.f;
+            for (long long q0 = c_first; q0 <= c_last; q0 += 4) {
+              float v[4][8];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const long long q = q0 + j;
+                if (q <= c_last) {
+                  const int qslot = ((long long)tile == stripe_begin(q, U, G) / KT) ? 0 : 1;
+                  const float* qp = p.partials + ((size_t)q * 2 + qslot) * ((size_t)p.bn * kTileN) +
+                                    (size_t)(cc * 8) * kTileN + row;
+#pragma unroll
+                  for (int c = 0; c < 8; ++c) v[j][c] = __ldcg(qp + (size_t)c * kTileN);
+                }
+              }
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                if (q0 + j <= c_last) {
+#pragma unroll
+                  for (int c = 0; c < 8; ++c) acc[c] += v[j][c];
+                }
+            }
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
               const int m = cc * 8 + c;
-              if (m_base + m >= p.M) continue;
-              float acc = 0.f;
-              for (long long q = c_first; q <= c_last; ++q) {
-                const int qslot = (tile == stripe_begin(q, U, G) / p.kt) ? 0 : 1;
-                const float* qp = p.partials + ((size_t)q * 2 + qslot) * ((size_t)p.bn * kTileN);
-                acc += __ldcg(qp + (size_t)m * kTileN + row);
-              }
-              p.Y[(size_t)(m_base + m) * p.N + y_col] = __half_as_ushort(__float2half_rn(acc));
+              if (m_base + m < p.M)
+                p.Y[(size_t)(m_base + m) * p.N + y_col] = __half_as_ushort(__float2half_rn(acc[c]));
             }
           }
         }
       }
       ++seg;
+      u += seg_len;
+      ku = 0;
+      ++tile;
     }
   }
 
   // ---- teardown -------------------------------------------------------------------
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 2) {
