@@ -61,9 +61,9 @@ const char* marlin_status_string(marlin_status_t status);
  * Size and offsets of the single repacked weight buffer, laid out as
  * [codes | scales | zeros]:
  *   codes  K*N/2 bytes in this library's tile layout (see marlin_repack);
- *   scales fp16 [K/group][N], verbatim, at *off_scales;
- *   zeros  int32 [K/group][N/8], verbatim, at *off_zeros (only if has_zeros;
- *          *off_zeros = *bytes otherwise).
+ *   scales fp16, K*N/group values, at *off_scales (tile-major, see marlin_repack);
+ *   zeros  K*N/(2*group) bytes at *off_zeros (only if has_zeros; *off_zeros =
+ *          *bytes otherwise), tile-major, see marlin_repack.
  * All offsets are multiples of 256 bytes.  Host-only, no CUDA call.
  * bytes, off_scales, off_zeros: host pointers, each may be NULL.
  */
@@ -81,10 +81,15 @@ marlin_status_t marlin_packed_layout(int K, int N, int group, int has_zeros, siz
  * zeros   device, int32 [K/group][N/8], or NULL for z = 8 (read only).
  * out     device, marlin_packed_layout(K, N, group, zeros != NULL) bytes,
  *         16-byte aligned, written.  Must not overlap the inputs.
- * Code layout in `out` (32-bit words):
- *   word ((nt*(K/64) + kb)*2 + h)*512 + nl*4 + i holds, at bits 4p..4p+3
- *   (p = 0..7), the code q[kb*64 + (h*4+i)*8 + koff(p)][nt*128 + nl] with
- *   koff(p) = 2p for p < 4 and 2(p-4)+1 for p >= 4.
+ * Layout of `out` (the operand order of a 16x16 fp16 tensor-core fragment):
+ *   codes   32-bit word ((nt*(K/64) + kb)*8 + g)*128 + l*4 + j, for nt < N/128,
+ *           kb < K/64, g < 8, l < 32, j < 4, holds at bits 4p..4p+3 (p = 0..7)
+ *           the code q[k][n] with n = nt*128 + 16g + l/4 + 8*(p & 1) and
+ *           k = kb*64 + 16j + 4*(l % 4) + 2*((p >> 1) & 1) + (p >> 2);
+ *   scales  fp16 [N/128][K/group][128] at off_scales: scale (gi, n) at
+ *           ((n/128)*(K/group) + gi)*128 + n%128;
+ *   zeros   bytes [N/128][K/group][64] at off_zeros: the 64-byte slice
+ *           zeros[gi][16*(n/128) .. 16*(n/128)+15] at ((n/128)*(K/group) + gi)*64.
  * Errors: INVALID_ARG (shape/group/NULL), MISALIGNED, CUDA (launch).
  */
 marlin_status_t marlin_repack(const int32_t* q, const uint16_t* scales, const int32_t* zeros, int K,
@@ -110,8 +115,8 @@ marlin_status_t marlin_workspace_bytes(int M, int K, int N, int group, int devic
  *
  * X          device, fp16 [M][K] row-major, 16-byte aligned (read only).
  * packed     device, the codes region of a marlin_repack output (offset 0).
- * scales     device, fp16 [K/group][N] (normally packed + off_scales).
- * zeros      device, int32 [K/group][N/8] (packed + off_zeros) or NULL (z = 8).
+ * scales     device, the scales region of the repacked buffer (packed + off_scales).
+ * zeros      device, the zeros region (packed + off_zeros), or NULL for z = 8.
  * Y          device, fp16 [M][N] row-major, written; must not overlap inputs.
  * workspace  device, >= marlin_workspace_bytes(...) bytes, 16-byte aligned.
  *            Zero it once after allocating; every call leaves it zeroed again.

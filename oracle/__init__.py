@@ -68,6 +68,10 @@ def _load():
         lib.oracle_w4a16.argtypes = [P, P, P, P, I, I, I, I, P, ctypes.c_int64, P, I]
         lib.oracle_repack.argtypes = [P, I, I, P]
         lib.oracle_unrepack.argtypes = [P, I, I, P]
+        lib.oracle_repack_scales.argtypes = [P, I, I, P]
+        lib.oracle_repack_zeros.argtypes = [P, I, I, P]
+        lib.oracle_repack_scales.restype = I
+        lib.oracle_repack_zeros.restype = I
         lib.oracle_round_array.argtypes = [P, ctypes.c_int64, P]
         lib.oracle_round_array.restype = None
         lib.oracle_widen_array.argtypes = [P, ctypes.c_int64, P]
@@ -185,6 +189,24 @@ def repack(Qp, K: int, N: int) -> np.ndarray:
     P = np.empty((N // 128) * (K // 64) * 1024, np.int32)
     assert _load().oracle_repack(_ptr(Qp), K, N, _ptr(P)) == 0
     return P
+
+
+def repack_scales(S, N: int) -> np.ndarray:
+    """fp16 scales [G][N] -> tile-major [N/128][G][128] (flattened, float16)."""
+    S = _bits16(S)
+    G = S.shape[0]
+    out = np.empty(G * N, np.uint16)
+    assert _load().oracle_repack_scales(_ptr(S), G, N, _ptr(out)) == 0
+    return out.view(np.float16)
+
+
+def repack_zeros(Zp, N: int) -> np.ndarray:
+    """Packed zeros int32 [G][N/8] -> tile-major bytes [N/128][G][64] (flattened uint8)."""
+    Zp = _i32(Zp)
+    G = Zp.shape[0]
+    out = np.zeros(G * N // 2, np.uint8)
+    assert _load().oracle_repack_zeros(_ptr(Zp), G, N, _ptr(out)) == 0
+    return out
 
 
 def unrepack(P, K: int, N: int) -> np.ndarray:

@@ -26,11 +26,15 @@
  * plus the tile layout of the repacked weights (the "reshuffle" of the pages:
  * "Marlin / GPTQ-Marlin", section "Tiled layout et repacking"; "Marlin Project
  * Overview" (vecbase.com), section "Key Techniques", item "Reshuffling").  The
- * repacked layout is this library's own; its index formula is:
- *   word index  = ((nt * (K/64) + kb) * 2 + h) * 512 + nl * 4 + i
- *   holds the 8 codes  q[kb*64 + (h*4+i)*8 + koff(p)][nt*128 + nl],  p = 0..7,
- *   code of nibble position p at bits 4p..4p+3, where koff(p) = 2p for p < 4
- *   and 2(p-4)+1 for p >= 4.
+ * repacked layout is this library's own, the operand order of a 16x16 fp16
+ * tensor-core fragment; its index formula is:
+ *   codes: word ((nt*(K/64) + kb)*8 + g)*128 + l*4 + j   (nt < N/128, kb < K/64,
+ *          g < 8, l < 32, j < 4) holds at bits 4p..4p+3 (p = 0..7) the code
+ *          q[k][n] with n = nt*128 + 16g + l/4 + 8*(p & 1),
+ *                      k = kb*64 + 16j + 4*(l % 4) + 2*((p >> 1) & 1) + (p >> 2);
+ *   scales: fp16 [N/128][K/g][128], scale (gi, n) at ((n/128)*(K/g) + gi)*128 + n%128;
+ *   zeros:  bytes [N/128][K/g][64], the 64-byte slice Zp[gi][16*(n/128) .. +15]
+ *           at ((n/128)*(K/g) + gi)*64.
  *
  * Build: gcc -O2 -ffp-contract=off -fPIC -shared -pthread (no FMA contraction,
  * so every sum rounds after each add, identically on x86-64 and aarch64).
@@ -248,9 +252,10 @@ int oracle_w4a16(const uint16_t* X, const int32_t* Qp, const uint16_t* S, const 
 
 /* ---- repacked tile layout ------------------------------------------------ */
 
-/* k offset, within a group of 8 consecutive k, of the code stored at nibble
- * position p of a repacked word. */
-static inline int koff(int p) { return p < 4 ? 2 * p : 2 * (p - 4) + 1; }
+/* Row (within the 128-column tile) and k (within the 64-row block) of nibble p
+ * of the word at (g, l, j) of a chunk. */
+static inline int frag_row(int g, int l, int p) { return 16 * g + l / 4 + 8 * (p & 1); }
+static inline int frag_k(int l, int j, int p) { return 16 * j + 4 * (l % 4) + 2 * ((p >> 1) & 1) + (p >> 2); }
 
 /* Qp [K/8][N] GPTQ order -> P [(N/128)*(K/64)*1024] words, tile layout. */
 int oracle_repack(const int32_t* Qp, int K, int N, int32_t* P) {
@@ -258,15 +263,16 @@ int oracle_repack(const int32_t* Qp, int K, int N, int32_t* P) {
   int KB = K / 64, NT = N / 128;
   for (int nt = 0; nt < NT; ++nt)
     for (int kb = 0; kb < KB; ++kb)
-      for (int h = 0; h < 2; ++h)
-        for (int nl = 0; nl < 128; ++nl)
-          for (int i = 0; i < 4; ++i) {
+      for (int g = 0; g < 8; ++g)
+        for (int l = 0; l < 32; ++l)
+          for (int j = 0; j < 4; ++j) {
             uint32_t word = 0;
             for (int p = 0; p < 8; ++p) {
-              int k = kb * 64 + (h * 4 + i) * 8 + koff(p);
-              word |= (uint32_t)code_at(Qp, N, k, nt * 128 + nl) << (4 * p);
+              int k = kb * 64 + frag_k(l, j, p);
+              int n = nt * 128 + frag_row(g, l, p);
+              word |= (uint32_t)code_at(Qp, N, k, n) << (4 * p);
             }
-            size_t at = ((size_t)(nt * KB + kb) * 2 + h) * 512 + (size_t)nl * 4 + i;
+            size_t at = ((size_t)(nt * KB + kb) * 8 + g) * 128 + (size_t)l * 4 + j;
             P[at] = (int32_t)word;
           }
   return 0;
@@ -279,18 +285,40 @@ int oracle_unrepack(const int32_t* P, int K, int N, int32_t* Qp) {
   memset(Qp, 0, sizeof(int32_t) * (size_t)(K / 8) * N);
   for (int nt = 0; nt < NT; ++nt)
     for (int kb = 0; kb < KB; ++kb)
-      for (int h = 0; h < 2; ++h)
-        for (int nl = 0; nl < 128; ++nl)
-          for (int i = 0; i < 4; ++i) {
-            size_t at = ((size_t)(nt * KB + kb) * 2 + h) * 512 + (size_t)nl * 4 + i;
+      for (int g = 0; g < 8; ++g)
+        for (int l = 0; l < 32; ++l)
+          for (int j = 0; j < 4; ++j) {
+            size_t at = ((size_t)(nt * KB + kb) * 8 + g) * 128 + (size_t)l * 4 + j;
             uint32_t word = (uint32_t)P[at];
             for (int p = 0; p < 8; ++p) {
-              int k = kb * 64 + (h * 4 + i) * 8 + koff(p);
-              int n = nt * 128 + nl;
+              int k = kb * 64 + frag_k(l, j, p);
+              int n = nt * 128 + frag_row(g, l, p);
               uint32_t q = (word >> (4 * p)) & 0xFu;
               Qp[(size_t)(k / 8) * N + n] |= (int32_t)(q << (4 * (k % 8)));
             }
           }
+  return 0;
+}
+
+/* Scales [G][N] fp16 bits -> tile-major [N/128][G][128]. */
+int oracle_repack_scales(const uint16_t* S, int G, int N, uint16_t* out) {
+  if (G <= 0 || N <= 0 || N % 128) return 1;
+  for (int gi = 0; gi < G; ++gi)
+    for (int n = 0; n < N; ++n)
+      out[((size_t)(n / 128) * G + gi) * 128 + n % 128] = S[(size_t)gi * N + n];
+  return 0;
+}
+
+/* Packed zeros [G][N/8] int32 -> tile-major bytes [N/128][G][64]. */
+int oracle_repack_zeros(const int32_t* Zp, int G, int N, uint8_t* out) {
+  if (G <= 0 || N <= 0 || N % 128) return 1;
+  for (int gi = 0; gi < G; ++gi)
+    for (int n = 0; n < N; ++n) {
+      int z = zero_at(Zp, N, gi, n);
+      uint8_t* b = out + ((size_t)(n / 128) * G + gi) * 64 + (n % 128) / 2;
+      if (n % 2 == 0) *b = (uint8_t)((*b & 0xF0) | z);
+      else *b = (uint8_t)((*b & 0x0F) | (z << 4));
+    }
   return 0;
 }
 

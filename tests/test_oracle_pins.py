@@ -240,15 +240,33 @@ def test_unpack_nibble_order():
 # ---- repacked layout ------------------------------------------------------------
 
 def test_repack_layout_literals():
-    """q[k][n] = k mod 16 (independent of n).  Word (nt, kb, h, n, i) holds the
-    codes of k = kb*64 + (h*4+i)*8 + koff(p) at nibble p, koff = 0,2,4,6,1,3,5,7."""
+    """Word (nt, kb, g, l, j) of the tile layout holds, at nibble p, the code of
+    row 16g + l/4 + 8(p&1) and k = 16j + 4(l%4) + 2((p>>1)&1) + (p>>2) of the
+    (nt, kb) tile.  Checked against words worked out by hand."""
     K, N = 128, 256
-    q = (np.arange(K) % 16)[:, None].repeat(N, 1)
-    P = oracle.repack(pack_codes(q), K, N).view(np.uint32).reshape(N // 128, K // 64, 2, 128, 4)
-    assert P[0, 0, 0, 0, 0] == 0x75316420      # k 0..7
-    assert P[0, 0, 0, 5, 1] == 0xFDB9ECA8      # k 8..15
-    assert P[1, 1, 1, 127, 3] == 0xFDB9ECA8    # k 64+56..64+63 -> codes 8..15
-    assert P[0, 0, 1, 3, 0] == 0x75316420      # k 32..39 -> codes 0..7
+    P = lambda q: oracle.repack(pack_codes(q), K, N).view(np.uint32).reshape(N // 128, K // 64, 8, 32, 4)
+    # q = k mod 16: only l % 4 matters -> nibbles (p7..p0) = 4c + (3,3,1,1,2,2,0,0)
+    Pk = P((np.arange(K) % 16)[:, None].repeat(N, 1))
+    assert Pk[0, 0, 0, 0, 0] == 0x33112200
+    assert Pk[1, 1, 5, 1, 3] == 0x77556644
+    assert Pk[0, 1, 7, 30, 2] == 0xBB99AA88
+    assert Pk[1, 0, 3, 7, 1] == 0xFFDDEECC
+    # q = n mod 16: only l / 4 matters -> even nibbles r = l/4, odd nibbles r + 8
+    Pn = P((np.arange(N) % 16)[None, :].repeat(K, 0))
+    assert Pn[0, 0, 2, 5, 0] == 0x91919191
+    assert Pn[1, 1, 6, 30, 3] == 0xF7F7F7F7
+
+
+def test_repack_scales_and_zeros_tile_major():
+    G, N = 3, 256
+    S = (np.arange(G * N, dtype=np.float64).reshape(G, N) / 64).astype(np.float16)
+    Sr = oracle.repack_scales(S, N).reshape(N // 128, G, 128)
+    assert Sr[1, 2, 5] == S[2, 128 + 5] and Sr[0, 1, 127] == S[1, 127]
+    z = (np.arange(G * N).reshape(G, N) * 7) % 16
+    Zr = oracle.repack_zeros(pack_zeros(z), N).reshape(N // 128, G, 64)
+    # byte b of tile row (nt, gi) holds columns 2b (low nibble) and 2b + 1 (high nibble)
+    assert Zr[1, 2, 3] == (z[2, 128 + 6] | (z[2, 128 + 7] << 4))
+    assert Zr[0, 0, 63] == (z[0, 126] | (z[0, 127] << 4))
 
 
 @pytest.mark.parametrize("K,N", [(128, 128), (256, 384), (4096, 4096), (11008, 256)])

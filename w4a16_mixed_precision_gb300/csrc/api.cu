@@ -142,8 +142,10 @@ marlin_status_t marlin_repack(const int32_t* q, const uint16_t* scales, const in
   if (launch_repack(reinterpret_cast<const uint32_t*>(q), reinterpret_cast<uint32_t*>(o), K, N, st) !=
       cudaSuccess)
     return MARLIN_ERR_CUDA;
-  if (launch_copy16(scales, o + off_s, G * N * 2, st) != cudaSuccess) return MARLIN_ERR_CUDA;
-  if (zeros && launch_copy16(zeros, o + off_z, G * N / 2, st) != cudaSuccess) return MARLIN_ERR_CUDA;
+  if (launch_tile_major(scales, o + off_s, (int)G, N, kTileN * 2, st) != cudaSuccess)
+    return MARLIN_ERR_CUDA;
+  if (zeros && launch_tile_major(zeros, o + off_z, (int)G, N, kTileN / 2, st) != cudaSuccess)
+    return MARLIN_ERR_CUDA;
   return MARLIN_OK;
 }
 
@@ -209,6 +211,7 @@ marlin_status_t marlin_gemm(const uint16_t* X, const void* packed, const uint16_
   p.K = K;
   p.N = N;
   p.group = group;
+  p.G = K / group;
   p.bn = g.bn;
   p.m_tiles = g.m_tiles;
   p.n_tiles = g.n_tiles;

@@ -123,25 +123,41 @@ __device__ __forceinline__ uint32_t as_u32(__half2 v) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// One 32-bit word of 8 codes -> 4 fp16 pairs (k, k+1), (k+2, k+3), ... scaled.
-// Nibble positions 0..3 hold k offsets 0, 2, 4, 6 and positions 4..7 hold
-// 1, 3, 5, 7, so a 0x000F000F mask pulls a consecutive pair into the low 4 bits
-// of each half.  0x6400 | c is 1024 + c exactly (binary16 ulp is 1 on
-// [1024, 2048)); 0x6400 | (c << 4) is 1024 + 16c.  Subtracting 1024 + z (or
-// scaling by 1/16 and adding -(64 + z)) gives q - z exactly; the single
-// rounding of the whole dequantisation is the final multiply by the scale.
-__device__ __forceinline__ void dequant_word(uint32_t w, __half2 sub_lo, __half2 add_hi,
-                                             __half2 s2, uint32_t* out) {
+// One 32-bit word of 8 codes -> the four fp16 pairs of a 16x16 operand
+// fragment: h[0] = column r, rows k..k+1; h[1] = column r+8, rows k..k+1;
+// h[2] = column r, rows k+2..k+3; h[3] = column r+8, rows k+2..k+3 (the
+// nibble order the repack writes).  0x6400 | c is 1024 + c exactly (binary16
+// ulp is 1 on [1024, 2048)); 0x6400 | (c << 4) is 1024 + 16c.  Subtracting
+// 1024 + z (or scaling by 1/16 and adding -(64 + z)) gives q - z exactly; the
+// single rounding of the dequantisation is the final multiply by the scale.
+__device__ __forceinline__ void dequant_frag(uint32_t w, __half2 sub_r, __half2 add_r8, __half2 s_r,
+                                             __half2 s_r8, uint32_t (&h)[4]) {
   const __half2 sixteenth = as_h2(0x2C002C00u);
   const uint32_t w8 = w >> 8;
   const uint32_t a = (w & 0x000F000Fu) | 0x64006400u;
   const uint32_t b = (w & 0x00F000F0u) | 0x64006400u;
   const uint32_t c = (w8 & 0x000F000Fu) | 0x64006400u;
   const uint32_t d = (w8 & 0x00F000F0u) | 0x64006400u;
-  out[0] = as_u32(__hmul2(__hsub2(as_h2(a), sub_lo), s2));
-  out[1] = as_u32(__hmul2(__hfma2(as_h2(b), sixteenth, add_hi), s2));
-  out[2] = as_u32(__hmul2(__hsub2(as_h2(c), sub_lo), s2));
-  out[3] = as_u32(__hmul2(__hfma2(as_h2(d), sixteenth, add_hi), s2));
+  h[0] = as_u32(__hmul2(__hsub2(as_h2(a), sub_r), s_r));
+  h[1] = as_u32(__hmul2(__hfma2(as_h2(b), sixteenth, add_r8), s_r8));
+  h[2] = as_u32(__hmul2(__hsub2(as_h2(c), sub_r), s_r));
+  h[3] = as_u32(__hmul2(__hfma2(as_h2(d), sixteenth, add_r8), s_r8));
+}
+
+// Per-column constants of the dequantisation: 1024 + z and -(64 + z) as fp16
+// pairs, and the scale broadcast to both halves.
+struct ColConst {
+  __half2 sub, add, s;
+};
+
+__device__ __forceinline__ ColConst col_const(uint16_t s_bits, uint32_t z) {
+  const uint32_t sub_u = 0x6400u | z;
+  const uint32_t add_u = 0xD400u | (z << 4);
+  ColConst k;
+  k.sub = as_h2(sub_u | (sub_u << 16));
+  k.add = as_h2(add_u | (add_u << 16));
+  k.s = as_h2((uint32_t)s_bits | ((uint32_t)s_bits << 16));
+  return k;
 }
 
 // ---- the kernel -----------------------------------------------------------------
@@ -228,11 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(fb, p.tx_bytes);
         bulk_g2s(st + p.off_codes, codes + ((size_t)nt * KB + (size_t)ku * cpu) * kChunkCodeBytes,
                  code_bytes, fb, pol_w);
-        bulk_g2s(st + p.off_scales, p.scales + (size_t)g * p.N + (size_t)nt * kTileN, kTileN * 2, fb,
-                 pol_w);
-        if (p.zeros)
-          bulk_g2s(st + p.off_zeros, p.zeros + (size_t)g * (p.N / 2) + (size_t)nt * (kTileN / 2),
-                   kTileN / 2, fb, pol_w);
+        const size_t grow = (size_t)nt * p.G + g;  // tile-major group row
+        bulk_g2s(st + p.off_scales, p.scales + grow * kTileN, kTileN * 2, fb, pol_w);
+        if (p.zeros) bulk_g2s(st + p.off_zeros, p.zeros + grow * (kTileN / 2), kTileN / 2, fb, pol_w);
         for (int j = 0; j < cpu; ++j)
           tma_load_2d(st + (uint32_t)j * p.x_chunk_bytes, &x_map, k0 + j * kChunkK, mt * p.bn, fb,
                       pol_x);
@@ -300,9 +314,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int dq = warp - kFirstDqWarp;       // 0..7
     const int wg = dq >> 2;                   // warpgroup: even / odd chunks
     const int quarter = warp & 3;             // TMEM lane quarter this warp may touch
-    const int row = quarter * 32 + lane;      // output column within the tile
+    const int row = quarter * 32 + lane;      // epilogue: output column within the tile
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const bool has_zeros = p.zeros != nullptr;
+    // dequantisation: this thread holds fragment lane `lane` of the two 16-column
+    // groups 2*quarter and 2*quarter+1, i.e. columns fr + {0, 8} of each
+    const int fr = lane >> 2;
     int s = 0, a = 0, ch = 0, seg = 0, npartial = 0;
     uint32_t ph = 0, aph = 0;
     int u = u_begin, ku = ku_begin, tile = tile_begin;
@@ -318,34 +335,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < cpu; ++j) {
           if ((ch & 1) == wg) {
             if (!wait_warp(bar(ctrl->full[s]), ph, ctrl, p)) { ok = false; break; }
-            const uint32_t cw = st + p.off_codes + (uint32_t)j * kChunkCodeBytes + (uint32_t)row * 16;
-            const uint4 lo = lds128(cw);
-            const uint4 hi = lds128(cw + 2048);
-            const uint16_t s_bits = reinterpret_cast<const uint16_t*>(st_ptr + p.off_scales)[row];
-            uint32_t z = 8;
-            if (has_zeros) z = (st_ptr[p.off_zeros + (row >> 1)] >> ((row & 1) * 4)) & 0xFu;
+            const uint32_t cw = st + p.off_codes + (uint32_t)j * kChunkCodeBytes +
+                                (uint32_t)((2 * quarter) * 32 + lane) * 16;
+            const uint4 w0 = lds128(cw);        // group 2q, k-steps 0..3
+            const uint4 w1 = lds128(cw + 512);  // group 2q+1
+            const uint16_t* sc = reinterpret_cast<const uint16_t*>(st_ptr + p.off_scales);
+            const int c0 = 32 * quarter + fr;   // columns c0, c0+8, c0+16, c0+24
+            uint32_t z0 = 8, z1 = 8, z2 = 8, z3 = 8;
+            if (has_zeros) {
+              const uint8_t* zb = st_ptr + p.off_zeros;
+              z0 = (zb[(c0) >> 1] >> ((c0 & 1) * 4)) & 0xFu;
+              z1 = (zb[(c0 + 8) >> 1] >> ((c0 & 1) * 4)) & 0xFu;
+              z2 = (zb[(c0 + 16) >> 1] >> ((c0 & 1) * 4)) & 0xFu;
+              z3 = (zb[(c0 + 24) >> 1] >> ((c0 & 1) * 4)) & 0xFu;
+            }
+            const ColConst k0 = col_const(sc[c0], z0), k1 = col_const(sc[c0 + 8], z1);
+            const ColConst k2 = col_const(sc[c0 + 16], z2), k3 = col_const(sc[c0 + 24], z3);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(ctrl->empty[s]));
 
-            const uint32_t s2u = (uint32_t)s_bits | ((uint32_t)s_bits << 16);
-            const uint32_t sub_u = 0x6400u | z;
-            const uint32_t add_u = 0xD400u | (z << 4);
-            const __half2 s2 = as_h2(s2u);
-            const __half2 sub_lo = as_h2(sub_u | (sub_u << 16));
-            const __half2 add_hi = as_h2(add_u | (add_u << 16));
-            uint32_t v[32];
-            dequant_word(lo.x, sub_lo, add_hi, s2, v + 0);
-            dequant_word(lo.y, sub_lo, add_hi, s2, v + 4);
-            dequant_word(lo.z, sub_lo, add_hi, s2, v + 8);
-            dequant_word(lo.w, sub_lo, add_hi, s2, v + 12);
-            dequant_word(hi.x, sub_lo, add_hi, s2, v + 16);
-            dequant_word(hi.y, sub_lo, add_hi, s2, v + 20);
-            dequant_word(hi.z, sub_lo, add_hi, s2, v + 24);
-            dequant_word(hi.w, sub_lo, add_hi, s2, v + 28);
+            // tcgen05.st.16x256b order per k-step: (col r, k..k+1), (col r, k+2..k+3),
+            // (col r+8, k..k+1), (col r+8, k+2..k+3)
+            uint32_t v0[16], v1[16];
+            const uint32_t wa[4] = {w0.x, w0.y, w0.z, w0.w};
+            const uint32_t wb[4] = {w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              uint32_t h[4];
+              dequant_frag(wa[ks], k0.sub, k1.add, k0.s, k1.s, h);
+              v0[4 * ks + 0] = h[0];
+              v0[4 * ks + 1] = h[2];
+              v0[4 * ks + 2] = h[1];
+              v0[4 * ks + 3] = h[3];
+              dequant_frag(wb[ks], k2.sub, k3.add, k2.s, k3.s, h);
+              v1[4 * ks + 0] = h[0];
+              v1[4 * ks + 1] = h[2];
+              v1[4 * ks + 2] = h[1];
+              v1[4 * ks + 3] = h[3];
+            }
 
             if (!wait_warp(bar(ctrl->aempty[a]), aph ^ 1u, ctrl, p)) { ok = false; break; }
             tc_fence_after();
-            tmem_st_x32(tmem + lane_off + kAColBase + (uint32_t)a * (kChunkK / 2), v);
+            const uint32_t acol = tmem + kAColBase + (uint32_t)a * (kChunkK / 2);
+            tmem_st_16x256b_x4(acol + lane_off, v0);
+            tmem_st_16x256b_x4(acol + lane_off + (16u << 16), v1);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();

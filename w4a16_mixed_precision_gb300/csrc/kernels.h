@@ -25,13 +25,13 @@ constexpr int kStatusTimeout = 1;
 
 struct GemmParams {
   const uint32_t* codes;    // tile-layout codes
-  const uint16_t* scales;   // fp16 [G][N]
-  const uint8_t* zeros;     // packed zeros [G][N/2 bytes] or nullptr
+  const uint16_t* scales;   // fp16, tile-major [N/128][G][128]
+  const uint8_t* zeros;     // zeros, tile-major bytes [N/128][G][64], or nullptr
   uint16_t* Y;              // fp16 [M][N]
   float* partials;          // [grid][2][bn][128] fp32
   int* counters;            // [m_tiles * n_tiles]
   int* status;              // status word
-  int M, K, N, group;
+  int M, K, N, group, G;
   int bn;                   // tokens per m-tile, multiple of 16
   int m_tiles, n_tiles;
   int kt;                   // units per tile along K
@@ -59,6 +59,8 @@ cudaError_t launch_gemm(const CUtensorMap& x_map, const GemmParams& p, int grid,
 cudaError_t gemm_set_smem_limit(int bytes);
 
 cudaError_t launch_repack(const uint32_t* q, uint32_t* out, int K, int N, cudaStream_t stream);
-cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, cudaStream_t stream);
+// Rows of row_bytes (multiple of 16) from [G][N/128][row] to [N/128][G][row].
+cudaError_t launch_tile_major(const void* src, void* dst, int G, int N, int row_bytes,
+                              cudaStream_t stream);
 
 }  // namespace w4a16
