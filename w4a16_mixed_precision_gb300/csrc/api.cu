@@ -2,6 +2,7 @@
 // partition plan, the X tensor map, and the kernel launches.
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "kernels.h"
@@ -65,27 +66,54 @@ bool normalise_group(int K, int* group) {
 
 bool valid_shape(int K, int N) { return K > 0 && N > 0 && K % 128 == 0 && N % 128 == 0; }
 
-// The partition plan.  bn = tokens per m-tile (UMMA N, multiple of 16, <= 256);
-// a unit is one (m-tile, 128-column tile, K slice of cpu*64); the grid is one
-// CTA per SM (fewer if there are fewer units), each taking an equal stripe.
-GemmPlan make_plan(int M, int K, int N, int sms, int smem_optin, bool has_zeros) {
+// Largest M served by the small-batch kernel (mma.sync path); larger M uses the
+// tcgen05 kernel.  W4A16_SMALL_M_MAX overrides it (0 disables the small path).
+int small_m_max() {
+  static int v = [] {
+    const char* e = getenv("W4A16_SMALL_M_MAX");
+    int x = e ? atoi(e) : 32;
+    return x < 0 ? 0 : (x > 32 ? 32 : x);
+  }();
+  return v;
+}
+
+// The partition plan.  A unit is one (m-tile, 128-column tile, K slice of
+// cpu*64 rows); the grid is one CTA per SM (fewer if there are fewer units),
+// each taking an equal contiguous stripe of units.
+GemmPlan make_plan(int M, int K, int N, int group, int sms, int smem_optin, bool has_zeros) {
   GemmPlan g{};
-  g.bn = M <= kMaxBn ? (int)round_up((size_t)M, 16) : kMaxBn;
-  if (g.bn < 16) g.bn = 16;
-  g.m_tiles = (M + g.bn - 1) / g.bn;
   g.n_tiles = N / kTileN;
-  g.cpu = g.bn <= 64 ? 2 : 1;
+  const int budget = smem_optin - kCtrlBytes - 1024;  // control block + alignment slack
+  if (M <= small_m_max()) {
+    // tokens in blocks of 8 (the mma.sync N dimension)
+    g.kind = kKernelSmallM;
+    g.bn = 8 * ((M + 7) / 8);
+    if (g.bn < 8) g.bn = 8;
+    g.m_tiles = 1;
+    const bool can4 = K % 256 == 0 && (group == 128 || group % 256 == 0);
+    const long long units4 = (long long)g.n_tiles * (K / 256);
+    g.cpu = (can4 && units4 >= 8LL * sms) ? 4 : 2;
+  } else {
+    g.kind = kKernelTcgen05;
+    g.bn = M <= kMaxBn ? (int)round_up((size_t)M, 16) : kMaxBn;
+    g.m_tiles = (M + g.bn - 1) / g.bn;
+    g.cpu = g.bn <= 64 ? 2 : 1;
+  }
   g.kt = K / (kChunkK * g.cpu);
+  g.n_g = (g.cpu * kChunkK > group) ? (g.cpu * kChunkK) / group : 1;
+  g.upg = (group > g.cpu * kChunkK) ? group / (g.cpu * kChunkK) : 1;
   g.units = (long long)g.m_tiles * g.n_tiles * g.kt;
   g.grid = (int)(g.units < sms ? g.units : sms);
   const size_t x_chunk = (size_t)g.bn * 128;
-  size_t stage = g.cpu * (x_chunk + kChunkCodeBytes) + kTileN * 2 + (has_zeros ? kTileN / 2 : 0);
+  const size_t stage = g.cpu * (x_chunk + kChunkCodeBytes) +
+                       (size_t)g.n_g * (kTileN * 2 + (has_zeros ? kTileN / 2 : 0));
   g.stage_bytes = (uint32_t)round_up(stage, 1024);
-  const int budget = smem_optin - kCtrlBytes - 1024;  // control block + alignment slack
-  int stages = budget / (int)g.stage_bytes;
+  const size_t xchg = g.kind == kKernelSmallM ? (size_t)4 * (g.bn / 8) * 256 * sizeof(float) : 0;
+  int stages = (int)((budget - (long long)xchg) / (long long)g.stage_bytes);
   if (stages > kMaxStages) stages = kMaxStages;
   g.stages = stages;
-  g.smem_bytes = (uint32_t)(kCtrlBytes + 1024 + (size_t)stages * g.stage_bytes);
+  g.off_xchg = (uint32_t)((size_t)stages * g.stage_bytes);
+  g.smem_bytes = (uint32_t)(kCtrlBytes + 1024 + (size_t)stages * g.stage_bytes + xchg);
   // workspace: [status 256 B][counters][partials]
   g.ws_counters_off = 256;
   g.ws_partials_off = round_up(g.ws_counters_off + sizeof(int) * (size_t)g.m_tiles * g.n_tiles, 256);
@@ -155,8 +183,14 @@ marlin_status_t marlin_workspace_bytes(int M, int K, int N, int group, int devic
   DeviceState* d;
   marlin_status_t s = device_state(device, &d);
   if (s != MARLIN_OK) return s;
-  const GemmPlan g = make_plan(M > 0 ? M : 1, K, N, d->sms, d->smem_optin, true);
-  *bytes = g.ws_bytes;
+  // the workspace must serve both kernels for every M' <= M
+  GemmPlan g = make_plan(M > 0 ? M : 1, K, N, group, d->sms, d->smem_optin, true);
+  size_t need = g.ws_bytes;
+  if (M > small_m_max() && small_m_max() > 0) {
+    const GemmPlan s = make_plan(small_m_max(), K, N, group, d->sms, d->smem_optin, true);
+    if (s.ws_bytes > need) need = s.ws_bytes;
+  }
+  *bytes = need;
   return MARLIN_OK;
 }
 
@@ -176,14 +210,16 @@ marlin_status_t marlin_gemm(const uint16_t* X, const void* packed, const uint16_
   if ((s = device_state(dev, &d)) != MARLIN_OK) return s;
   if ((s = get_encoder()) != MARLIN_OK) return s;
 
-  const GemmPlan g = make_plan(M, K, N, d->sms, d->smem_optin, zeros != nullptr);
+  const GemmPlan g = make_plan(M, K, N, group, d->sms, d->smem_optin, zeros != nullptr);
   if (g.stages < 2 || g.units > 0x7FFFFFFFLL / 2) return MARLIN_ERR_UNSUPPORTED;
   if (workspace_bytes < g.ws_bytes) return MARLIN_ERR_WORKSPACE_TOO_SMALL;
 
   {
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!d->smem_set) {
-      if (gemm_set_smem_limit(d->smem_optin) != cudaSuccess) return MARLIN_ERR_CUDA;
+      if (gemm_set_smem_limit(d->smem_optin) != cudaSuccess ||
+          small_m_set_smem_limit(d->smem_optin) != cudaSuccess)
+        return MARLIN_ERR_CUDA;
       d->smem_set = true;
     }
   }
@@ -223,14 +259,18 @@ marlin_status_t marlin_gemm(const uint16_t* X, const void* packed, const uint16_
   p.x_chunk_bytes = (uint32_t)g.bn * 128;
   p.off_codes = (uint32_t)g.cpu * p.x_chunk_bytes;
   p.off_scales = p.off_codes + (uint32_t)g.cpu * kChunkCodeBytes;
-  p.off_zeros = p.off_scales + kTileN * 2;
+  p.off_zeros = p.off_scales + (uint32_t)g.n_g * kTileN * 2;
   p.tx_bytes = (uint32_t)g.cpu * (p.x_chunk_bytes + kChunkCodeBytes) + kTileN * 2 +
                (zeros ? kTileN / 2 : 0);
   p.weights_reused = g.m_tiles > 1;
+  p.n_g = g.n_g;
+  p.units_per_group = g.upg;
+  p.off_xchg = g.off_xchg;
   p.timeout_ns = kDefaultTimeoutNs;
-  if (launch_gemm(x_map, p, g.grid, g.smem_bytes, reinterpret_cast<cudaStream_t>(stream)) !=
-      cudaSuccess)
-    return MARLIN_ERR_CUDA;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t e = g.kind == kKernelSmallM ? launch_small_m(x_map, p, g.grid, g.smem_bytes, st)
+                                                : launch_gemm(x_map, p, g.grid, g.smem_bytes, st);
+  if (e != cudaSuccess) return MARLIN_ERR_CUDA;
   return MARLIN_OK;
 }
 

@@ -1,0 +1,126 @@
+// common.cuh -- device helpers shared by the fused kernels: bounded mbarrier
+// waits, the striped partition arithmetic, and the exact 4-bit -> fp16
+// dequantisation of one operand fragment.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace w4a16 {
+
+// Where a CTA records that it gave up: a shared abort flag (so the other roles
+// stop quickly), the device status word, and the per-wait time limit.
+struct WaitCtx {
+  int* abort;
+  int* status;
+  unsigned long long timeout_ns;
+};
+
+// ---- bounded waits ----------------------------------------------------------
+// Each wait sleeps inside mbarrier.try_wait (woken when the phase completes)
+// and checks the abort flag and the global timer between sleeps.  The loops
+// are kept small and not unrolled: the kernel's roles run different code and
+// share one instruction cache.
+
+static __device__ __noinline__ void raise_timeout(const WaitCtx& c) {
+  *reinterpret_cast<volatile int*>(c.abort) = 1;
+  atomicOr(c.status, kStatusTimeout);
+}
+
+// Slow path of a wait: returns false when the CTA is aborting or the wait expired.
+static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& c) {
+  const uint64_t t0 = global_timer_ns();
+#pragma unroll 1
+  while (!mbar_try_wait(bar, parity)) {
+    if (*reinterpret_cast<volatile int*>(c.abort)) return false;
+    if (global_timer_ns() - t0 > c.timeout_ns) {
+      raise_timeout(c);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ bool wait_thread(uint32_t bar, uint32_t parity, const WaitCtx& c) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, c);
+}
+
+// Whole-warp wait with a warp-uniform outcome.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtx& c) {
+  return __all_sync(0xffffffffu, wait_thread(bar, parity, c));
+}
+
+// Wait used while tearing down: ignores the abort flag, still bounded.
+static __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, const WaitCtx& c) {
+  const uint64_t t0 = global_timer_ns();
+#pragma unroll 1
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > c.timeout_ns) {
+      atomicOr(c.status, kStatusTimeout);
+      return;
+    }
+  }
+}
+
+// ---- striped partition --------------------------------------------------------
+
+// First unit of CTA c's stripe: floor(c * U / G).
+__device__ __forceinline__ long long stripe_begin(long long c, long long U, long long G) {
+  return (c * U) / G;
+}
+
+// CTA whose stripe holds unit u (every stripe is non-empty because G <= U).
+__device__ __forceinline__ long long stripe_owner(long long u, long long U, long long G) {
+  return ((u + 1) * G - 1) / U;
+}
+
+// ---- dequantisation -------------------------------------------------------------
+
+__device__ __forceinline__ __half2 as_h2(uint32_t v) {
+  return *reinterpret_cast<__half2*>(&v);
+}
+__device__ __forceinline__ uint32_t as_u32(__half2 v) {
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// One 32-bit word of 8 codes -> the four fp16 pairs of a 16x16 operand
+// fragment: h[0] = column r, rows k..k+1; h[1] = column r+8, rows k..k+1;
+// h[2] = column r, rows k+2..k+3; h[3] = column r+8, rows k+2..k+3 (the
+// nibble order the repack writes).  0x6400 | c is 1024 + c exactly (binary16
+// ulp is 1 on [1024, 2048)); 0x6400 | (c << 4) is 1024 + 16c.  Subtracting
+// 1024 + z (or scaling by 1/16 and adding -(64 + z)) gives q - z exactly; the
+// single rounding of the dequantisation is the final multiply by the scale.
+__device__ __forceinline__ void dequant_frag(uint32_t w, __half2 sub_r, __half2 add_r8, __half2 s_r,
+                                             __half2 s_r8, uint32_t (&h)[4]) {
+  const __half2 sixteenth = as_h2(0x2C002C00u);
+  const uint32_t w8 = w >> 8;
+  const uint32_t a = (w & 0x000F000Fu) | 0x64006400u;
+  const uint32_t b = (w & 0x00F000F0u) | 0x64006400u;
+  const uint32_t c = (w8 & 0x000F000Fu) | 0x64006400u;
+  const uint32_t d = (w8 & 0x00F000F0u) | 0x64006400u;
+  h[0] = as_u32(__hmul2(__hsub2(as_h2(a), sub_r), s_r));
+  h[1] = as_u32(__hmul2(__hfma2(as_h2(b), sixteenth, add_r8), s_r8));
+  h[2] = as_u32(__hmul2(__hsub2(as_h2(c), sub_r), s_r));
+  h[3] = as_u32(__hmul2(__hfma2(as_h2(d), sixteenth, add_r8), s_r8));
+}
+
+// Per-column constants of the dequantisation: 1024 + z and -(64 + z) as fp16
+// pairs, and the scale broadcast to both halves.
+struct ColConst {
+  __half2 sub, add, s;
+};
+
+__device__ __forceinline__ ColConst col_const(uint16_t s_bits, uint32_t z) {
+  const uint32_t sub_u = 0x6400u | z;
+  const uint32_t add_u = 0xD400u | (z << 4);
+  ColConst k;
+  k.sub = as_h2(sub_u | (sub_u << 16));
+  k.add = as_h2(add_u | (add_u << 16));
+  k.s = as_h2((uint32_t)s_bits | ((uint32_t)s_bits << 16));
+  return k;
+}
+
+}  // namespace w4a16

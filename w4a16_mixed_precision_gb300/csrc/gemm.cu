@@ -27,8 +27,7 @@
 //     TMEM and returns.
 #include <cuda_fp16.h>
 
-#include "kernels.h"
-#include "ptx.cuh"
+#include "common.cuh"
 
 namespace w4a16 {
 
@@ -52,113 +51,6 @@ static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
 
 constexpr int kNumDqWarps = 8;
 constexpr int kFirstDqWarp = 4;
-
-// ---- bounded waits ----------------------------------------------------------
-// Each wait sleeps inside mbarrier.try_wait (woken when the phase completes)
-// and checks the abort flag and the global timer between sleeps.  The loops
-// are kept small and not unrolled: the kernel's roles run different code and
-// share one instruction cache.
-
-__device__ __noinline__ void raise_timeout(Ctrl* c, const GemmParams& p) {
-  *reinterpret_cast<volatile int*>(&c->abort) = 1;
-  atomicOr(p.status, kStatusTimeout);
-}
-
-// Slow path of a wait: returns false when the CTA is aborting or the wait expired.
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, Ctrl* c, const GemmParams& p) {
-  const uint64_t t0 = global_timer_ns();
-#pragma unroll 1
-  while (!mbar_try_wait(bar, parity)) {
-    if (*reinterpret_cast<volatile int*>(&c->abort)) return false;
-    if (global_timer_ns() - t0 > p.timeout_ns) {
-      raise_timeout(c, p);
-      return false;
-    }
-  }
-  return true;
-}
-
-__device__ __forceinline__ bool wait_thread(uint32_t bar, uint32_t parity, Ctrl* c,
-                                            const GemmParams& p) {
-  if (mbar_try_wait(bar, parity)) return true;
-  return wait_slow(bar, parity, c, p);
-}
-
-// Whole-warp wait with a warp-uniform outcome.
-__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, Ctrl* c,
-                                          const GemmParams& p) {
-  return __all_sync(0xffffffffu, wait_thread(bar, parity, c, p));
-}
-
-// Wait used while tearing down: ignores the abort flag, still bounded.
-__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, const GemmParams& p) {
-  const uint64_t t0 = global_timer_ns();
-#pragma unroll 1
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > p.timeout_ns) {
-      atomicOr(p.status, kStatusTimeout);
-      return;
-    }
-  }
-}
-
-// ---- striped partition --------------------------------------------------------
-
-// First unit of CTA c's stripe: floor(c * U / G).
-__device__ __forceinline__ long long stripe_begin(long long c, long long U, long long G) {
-  return (c * U) / G;
-}
-
-// CTA whose stripe holds unit u (every stripe is non-empty because G <= U).
-__device__ __forceinline__ long long stripe_owner(long long u, long long U, long long G) {
-  return ((u + 1) * G - 1) / U;
-}
-
-// ---- dequantisation -------------------------------------------------------------
-
-__device__ __forceinline__ __half2 as_h2(uint32_t v) {
-  return *reinterpret_cast<__half2*>(&v);
-}
-__device__ __forceinline__ uint32_t as_u32(__half2 v) {
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// One 32-bit word of 8 codes -> the four fp16 pairs of a 16x16 operand
-// fragment: h[0] = column r, rows k..k+1; h[1] = column r+8, rows k..k+1;
-// h[2] = column r, rows k+2..k+3; h[3] = column r+8, rows k+2..k+3 (the
-// nibble order the repack writes).  0x6400 | c is 1024 + c exactly (binary16
-// ulp is 1 on [1024, 2048)); 0x6400 | (c << 4) is 1024 + 16c.  Subtracting
-// 1024 + z (or scaling by 1/16 and adding -(64 + z)) gives q - z exactly; the
-// single rounding of the dequantisation is the final multiply by the scale.
-__device__ __forceinline__ void dequant_frag(uint32_t w, __half2 sub_r, __half2 add_r8, __half2 s_r,
-                                             __half2 s_r8, uint32_t (&h)[4]) {
-  const __half2 sixteenth = as_h2(0x2C002C00u);
-  const uint32_t w8 = w >> 8;
-  const uint32_t a = (w & 0x000F000Fu) | 0x64006400u;
-  const uint32_t b = (w & 0x00F000F0u) | 0x64006400u;
-  const uint32_t c = (w8 & 0x000F000Fu) | 0x64006400u;
-  const uint32_t d = (w8 & 0x00F000F0u) | 0x64006400u;
-  h[0] = as_u32(__hmul2(__hsub2(as_h2(a), sub_r), s_r));
-  h[1] = as_u32(__hmul2(__hfma2(as_h2(b), sixteenth, add_r8), s_r8));
-  h[2] = as_u32(__hmul2(__hsub2(as_h2(c), sub_r), s_r));
-  h[3] = as_u32(__hmul2(__hfma2(as_h2(d), sixteenth, add_r8), s_r8));
-}
-
-// Per-column constants of the dequantisation: 1024 + z and -(64 + z) as fp16
-// pairs, and the scale broadcast to both halves.
-struct ColConst {
-  __half2 sub, add, s;
-};
-
-__device__ __forceinline__ ColConst col_const(uint16_t s_bits, uint32_t z) {
-  const uint32_t sub_u = 0x6400u | z;
-  const uint32_t add_u = 0xD400u | (z << 4);
-  ColConst k;
-  k.sub = as_h2(sub_u | (sub_u << 16));
-  k.add = as_h2(add_u | (add_u << 16));
-  k.s = as_h2((uint32_t)s_bits | ((uint32_t)s_bits << 16));
-  return k;
-}
 
 // ---- the kernel -----------------------------------------------------------------
 //
@@ -190,6 +82,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ku_begin = u_begin - tile_begin * KT;
 
   auto bar = [&](const uint64_t& b) { return smem_addr(&b); };
+  const WaitCtx wc{&ctrl->abort, p.status, p.timeout_ns};
 
   // ---- setup --------------------------------------------------------------------
   if (warp == 0 && lane == 0) {
@@ -237,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;
       int issued = 0;
       for (int u = u_begin; u < u_end; ++u) {
-        if (!wait_thread(bar(ctrl->empty[s]), ph ^ 1u, ctrl, p)) break;
+        if (!wait_thread(bar(ctrl->empty[s]), ph ^ 1u, wc)) break;
         const int k0 = ku * cpu * kChunkK;
         const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
         const uint32_t fb = bar(ctrl->full[s]);
@@ -261,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Wait for every copy still in flight before the CTA may exit.
       const int first = issued > S ? issued - S : 0;
       for (int i = first; i < issued; ++i)
-        wait_drain(bar(ctrl->full[i % S]), (uint32_t)((i / S) & 1), p);
+        wait_drain(bar(ctrl->full[i % S]), (uint32_t)((i / S) & 1), wc);
     }
   } else if (warp == 1) {
     // ================= MMA issuer (one thread) =================
@@ -274,15 +167,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ok && u < u_end) {
         const int seg_len = min(u_end - u, KT - ku);
         if (seg > 0) {
-          if (!wait_thread(bar(ctrl->dempty), (uint32_t)((seg - 1) & 1), ctrl, p)) break;
+          if (!wait_thread(bar(ctrl->dempty), (uint32_t)((seg - 1) & 1), wc)) break;
           tc_fence_after();
         }
         uint32_t acc = 0;
         for (int i = 0; i < seg_len && ok; ++i) {
-          if (!wait_thread(bar(ctrl->full[s]), ph, ctrl, p)) { ok = false; break; }
+          if (!wait_thread(bar(ctrl->full[s]), ph, wc)) { ok = false; break; }
           const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
           for (int j = 0; j < cpu; ++j) {
-            if (!wait_thread(bar(ctrl->afull[a]), aph, ctrl, p)) { ok = false; break; }
+            if (!wait_thread(bar(ctrl->afull[a]), aph, wc)) { ok = false; break; }
             tc_fence_after();
             const uint32_t xs = st + (uint32_t)j * p.x_chunk_bytes;
             const uint32_t a_col = tmem + kAColBase + (uint32_t)a * (kChunkK / 2);
@@ -307,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Every issued MMA must finish before TMEM is released.
       mma_commit(bar(ctrl->drain));
-      wait_drain(bar(ctrl->drain), 0, p);
+      wait_drain(bar(ctrl->drain), 0, wc);
     }
   } else if (warp >= kFirstDqWarp) {
     // ================= dequantisation + epilogue (8 warps) =================
@@ -334,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t* st_ptr = stage0_ptr + (size_t)s * p.stage_bytes;
         for (int j = 0; j < cpu; ++j) {
           if ((ch & 1) == wg) {
-            if (!wait_warp(bar(ctrl->full[s]), ph, ctrl, p)) { ok = false; break; }
+            if (!wait_warp(bar(ctrl->full[s]), ph, wc)) { ok = false; break; }
             const uint32_t cw = st + p.off_codes + (uint32_t)j * kChunkCodeBytes +
                                 (uint32_t)((2 * quarter) * 32 + lane) * 16;
             const uint4 w0 = lds128(cw);        // group 2q, k-steps 0..3
@@ -374,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               v1[4 * ks + 3] = h[3];
             }
 
-            if (!wait_warp(bar(ctrl->aempty[a]), aph ^ 1u, ctrl, p)) { ok = false; break; }
+            if (!wait_warp(bar(ctrl->aempty[a]), aph ^ 1u, wc)) { ok = false; break; }
             tc_fence_after();
             const uint32_t acol = tmem + kAColBase + (uint32_t)a * (kChunkK / 2);
             tmem_st_16x256b_x4(acol + lane_off, v0);
@@ -392,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
 
       // ---- epilogue: accumulators -> fp16 Y, or fp32 partial tile ----
-      if (!wait_warp(bar(ctrl->dfull), (uint32_t)(seg & 1), ctrl, p)) break;
+      if (!wait_warp(bar(ctrl->dfull), (uint32_t)(seg & 1), wc)) break;
       tc_fence_after();
       const bool whole = (ku == 0 && seg_len == KT);
       const int slot = (tile == tile_begin) ? 0 : 1;
@@ -429,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const long long c_first = stripe_owner((long long)tile * KT, U, G);
         const long long c_last = stripe_owner((long long)tile * KT + KT - 1, U, G);
         if (dq == 0) {
-          if (!wait_warp(bar(ctrl->red_arrive), rph, ctrl, p)) break;
+          if (!wait_warp(bar(ctrl->red_arrive), rph, wc)) break;
           if (lane == 0) {
             __threadfence();
             const int expected = (int)(c_last - c_first + 1);
@@ -444,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
         }
-        if (!wait_warp(bar(ctrl->red_go), rph, ctrl, p)) break;
+        if (!wait_warp(bar(ctrl->red_go), rph, wc)) break;
         ++npartial;
         if (*reinterpret_cast<volatile int*>(&ctrl->reduce_last)) {
           // Sum the contributors' partial tiles in stripe order (fixed, so the

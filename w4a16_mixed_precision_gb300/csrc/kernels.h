@@ -43,12 +43,18 @@ struct GemmParams {
   uint32_t off_codes, off_scales, off_zeros;  // byte offsets inside a stage
   uint32_t tx_bytes;        // bytes landed per stage
   int weights_reused;       // more than one m-tile reads the same weights
+  int n_g;                  // scale/zero group rows per unit (2 only for group 128, 256-row units)
+  int units_per_group;      // units per group row (>= 1)
+  uint32_t off_xchg;        // small-M kernel: exchange buffer, bytes after stage 0
   unsigned long long timeout_ns;
 };
 
 // Partition and resource plan of one marlin_gemm call.
+enum KernelKind { kKernelTcgen05 = 0, kKernelSmallM = 1 };
 struct GemmPlan {
-  int bn, m_tiles, n_tiles, kt, cpu, stages, grid;
+  int kind;
+  int bn, m_tiles, n_tiles, kt, cpu, stages, grid, n_g, upg;
+  uint32_t off_xchg;
   long long units;
   uint32_t stage_bytes, smem_bytes;
   size_t ws_counters_off, ws_partials_off, ws_bytes;
@@ -57,6 +63,9 @@ struct GemmPlan {
 cudaError_t launch_gemm(const CUtensorMap& x_map, const GemmParams& p, int grid, uint32_t smem_bytes,
                         cudaStream_t stream);
 cudaError_t gemm_set_smem_limit(int bytes);
+cudaError_t launch_small_m(const CUtensorMap& x_map, const GemmParams& p, int grid,
+                           uint32_t smem_bytes, cudaStream_t stream);
+cudaError_t small_m_set_smem_limit(int bytes);
 
 cudaError_t launch_repack(const uint32_t* q, uint32_t* out, int K, int N, cudaStream_t stream);
 // Rows of row_bytes (multiple of 16) from [G][N/128][row] to [N/128][G][row].

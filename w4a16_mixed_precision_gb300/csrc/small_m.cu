@@ -1,0 +1,375 @@
+// small_m.cu -- the fused W4A16 matrix multiply for small batches (M <= 32):
+// Y[M][N] = X[M][K] . dequant(W)[K][N] on the warp-level tensor-core path.
+//
+// At M <= 32 the multiply is bound by streaming the 4-bit weights from HBM, and
+// the work per byte is the dequantisation ("Marlin", section "诞生背景": at
+// batch 8-16 earlier kernels lost the 4x because dequantisation was not
+// pipelined with the GEMM).  Here every consumer warp turns its own fragment
+// words into fp16 tensor-core operands in registers and feeds them to
+// mma.sync.m16n8k16 immediately ("Marlin", section "反量化与 GEMM 融合":
+// dequantise in registers, then the tensor core, no intermediate in memory);
+// no single thread issues MMAs for the whole SM and nothing is staged in TMEM.
+//
+//   * One persistent CTA per SM takes an equal stripe of (128-column tile,
+//     K-slice) units ("Marlin Project Overview", section "Key Techniques",
+//     item "Striped Partitioning"); tiles cut by a stripe boundary are summed by
+//     the last CTA to store its fp32 partial, in a fixed order.
+//   * Warp 0 streams the weights (codes, scales, zeros: one bulk copy each per
+//     unit) and warp 1 streams X (tensor copies, 128-byte swizzle) into a ring
+//     of mbarrier-guarded stages.
+//   * Warps 2..17: consumer warp (g, h) owns columns 16g..16g+15 of the tile
+//     and the 64-row chunks of parity h of every unit ("Marlin Project
+//     Overview", item "Warp Utilization": several warps compute partial results
+//     of one output tile); the two halves are summed through shared memory at
+//     the end of each tile.
+//   * The MMA's k order is permuted consistently for both operands: lane l
+//     holds rows 4(l%4)..4(l%4)+3 of every 16-row step (the repacked fragment
+//     order), so its X operand is one 8-byte shared load per step and token
+//     block.
+//   * Every wait is bounded; on expiry the kernel records a timeout in the
+//     status word and returns.
+#include "common.cuh"
+
+namespace w4a16 {
+
+namespace {
+
+constexpr int kSmConsumers = 16;
+constexpr int kSmThreads = (2 + kSmConsumers) * 32;
+
+struct SmCtrl {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t red_full;    // odd-half warps -> even-half warps: accumulators in smem
+  uint64_t red_free;    // even-half warps -> odd-half warps: exchange buffer read
+  uint64_t red_arrive;  // even-half warps -> leader: partial tile stored
+  uint64_t red_go;      // leader -> even-half warps: arrival counted
+  int abort;
+  int reduce_last;
+};
+static_assert(sizeof(SmCtrl) <= kCtrlBytes, "control block too large");
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+
+template <int NB>
+__global__ void __launch_bounds__(kSmThreads, 1)
+    w4a16_small_m_kernel(const __grid_constant__ CUtensorMap x_map, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
+  uint8_t* base = smem_raw + (base_addr - raw_addr);
+  SmCtrl* ctrl = reinterpret_cast<SmCtrl*>(base);
+  const uint32_t stage0 = base_addr + kCtrlBytes;
+  const uint8_t* stage0_ptr = base + kCtrlBytes;
+  float* xchg = reinterpret_cast<float*>(base + kCtrlBytes + p.off_xchg);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long U = p.units;
+  const long long G = gridDim.x;
+  const int u_begin = (int)stripe_begin(blockIdx.x, U, G);
+  const int u_end = (int)stripe_begin(blockIdx.x + 1, U, G);
+  const int KT = p.kt;
+  const int S = p.stages;
+  const int cpu = p.cpu;
+  const int tile_begin = u_begin / KT;
+  const int ku_begin = u_begin - tile_begin * KT;
+
+  auto bar = [&](const uint64_t& b) { return smem_addr(&b); };
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar(ctrl->full[s]), 2);
+      mbar_init(bar(ctrl->empty[s]), kSmConsumers);
+    }
+    mbar_init(bar(ctrl->red_full), kSmConsumers / 2);
+    mbar_init(bar(ctrl->red_free), kSmConsumers / 2);
+    mbar_init(bar(ctrl->red_arrive), kSmConsumers / 2);
+    mbar_init(bar(ctrl->red_go), 1);
+    ctrl->abort = 0;
+    ctrl->reduce_last = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 1 && lane == 0) prefetch_tensormap(&x_map);
+  __syncthreads();
+  const WaitCtx wc{&ctrl->abort, p.status, p.timeout_ns};
+
+  if (warp == 0) {
+    // ================= weights producer =================
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      const uint8_t* codes = reinterpret_cast<const uint8_t*>(p.codes);
+      const int KB = p.K / kChunkK;
+      const uint32_t code_bytes = (uint32_t)(cpu * kChunkCodeBytes);
+      const uint32_t scale_bytes = (uint32_t)(p.n_g * kTileN * 2);
+      const uint32_t zero_bytes = (uint32_t)(p.n_g * kTileN / 2);
+      const uint32_t tx = code_bytes + scale_bytes + (p.zeros ? zero_bytes : 0u);
+      const int upg = p.units_per_group;
+      int nt = tile_begin, ku = ku_begin;
+      int g = (ku / upg) * p.n_g, ku_in_g = ku - (ku / upg) * upg;
+      int s = 0, issued = 0;
+      uint32_t ph = 0;
+      for (int u = u_begin; u < u_end; ++u) {
+        if (!wait_thread(bar(ctrl->empty[s]), ph ^ 1u, wc)) break;
+        const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
+        const uint32_t fb = bar(ctrl->full[s]);
+        mbar_arrive_expect_tx(fb, tx);
+        bulk_g2s(st + p.off_codes, codes + ((size_t)nt * KB + (size_t)ku * cpu) * kChunkCodeBytes,
+                 code_bytes, fb, pol);
+        const size_t grow = (size_t)nt * p.G + g;
+        bulk_g2s(st + p.off_scales, p.scales + grow * kTileN, scale_bytes, fb, pol);
+        if (p.zeros) bulk_g2s(st + p.off_zeros, p.zeros + grow * (kTileN / 2), zero_bytes, fb, pol);
+        ++issued;
+        if (++s == S) { s = 0; ph ^= 1u; }
+        if (++ku_in_g == upg) { ku_in_g = 0; g += p.n_g; }
+        if (++ku == KT) { ku = 0; g = 0; ku_in_g = 0; ++nt; }
+      }
+      const int first = issued > S ? issued - S : 0;
+      for (int i = first; i < issued; ++i)
+        wait_drain(bar(ctrl->full[i % S]), (uint32_t)((i / S) & 1), wc);
+    }
+  } else if (warp == 1) {
+    // ================= activation producer =================
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_last();
+      const uint32_t tx = (uint32_t)cpu * p.x_chunk_bytes;
+      int ku = ku_begin;
+      int s = 0, issued = 0;
+      uint32_t ph = 0;
+      for (int u = u_begin; u < u_end; ++u) {
+        if (!wait_thread(bar(ctrl->empty[s]), ph ^ 1u, wc)) break;
+        const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
+        const uint32_t fb = bar(ctrl->full[s]);
+        mbar_arrive_expect_tx(fb, tx);
+        const int k0 = ku * cpu * kChunkK;
+        for (int j = 0; j < cpu; ++j)
+          tma_load_2d(st + (uint32_t)j * p.x_chunk_bytes, &x_map, k0 + j * kChunkK, 0, fb, pol);
+        ++issued;
+        if (++s == S) { s = 0; ph ^= 1u; }
+        if (++ku == KT) ku = 0;
+      }
+      const int first = issued > S ? issued - S : 0;
+      for (int i = first; i < issued; ++i)
+        wait_drain(bar(ctrl->full[i % S]), (uint32_t)((i / S) & 1), wc);
+    }
+  } else {
+    // ================= consumers =================
+    const int cw = warp - 2;
+    const int g = cw & 7;      // column group: tile columns 16g .. 16g + 15
+    const int h = cw >> 3;     // K-half: chunks of parity h
+    const int r = lane >> 2;   // fragment row / token column within a block of 8
+    const int c = lane & 3;
+    const int col_r = 16 * g + r;  // this lane's two tile columns: col_r, col_r + 8
+    const bool has_zeros = p.zeros != nullptr;
+    float acc[NB][4];
+    int s = 0, seg = 0, npartial = 0;
+    uint32_t ph = 0;
+    int u = u_begin, ku = ku_begin, tile = tile_begin;
+    bool ok = true;
+    while (ok && u < u_end) {
+      const int seg_len = min(u_end - u, KT - ku);
+      const bool whole = (ku == 0 && seg_len == KT);
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int d = 0; d < 4; ++d) acc[nb][d] = 0.f;
+
+      for (int i = 0; i < seg_len; ++i) {
+        if (!wait_warp(bar(ctrl->full[s]), ph, wc)) { ok = false; break; }
+        const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
+        const uint8_t* st_ptr = stage0_ptr + (size_t)s * p.stage_bytes;
+        for (int j = h; j < cpu; j += 2) {
+          const uint4 wv = lds128(st + p.off_codes + (uint32_t)j * kChunkCodeBytes +
+                                  (uint32_t)(g * 32 + lane) * 16);
+          const int gsub = (p.n_g > 1) ? (j >> 1) : 0;
+          const uint16_t* sc = reinterpret_cast<const uint16_t*>(st_ptr + p.off_scales) + gsub * kTileN;
+          uint32_t z0 = 8, z1 = 8;
+          if (has_zeros) {
+            const uint8_t* zb = st_ptr + p.off_zeros + gsub * (kTileN / 2);
+            z0 = (zb[col_r >> 1] >> ((col_r & 1) * 4)) & 0xFu;
+            z1 = (zb[(col_r + 8) >> 1] >> ((col_r & 1) * 4)) & 0xFu;
+          }
+          const ColConst k0 = col_const(sc[col_r], z0), k1 = col_const(sc[col_r + 8], z1);
+          const uint32_t xs = st + (uint32_t)j * p.x_chunk_bytes;
+          const uint32_t wk[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            uint32_t a[4];
+            dequant_frag(wk[ks], k0.sub, k1.add, k0.s, k1.s, a);
+            // X rows 8nb + r, k = 16ks + 4c .. +3: 16-byte chunk 2ks + c/2 of the
+            // 128-byte row, swizzled by the row index mod 8 (= r)
+            const uint32_t koff = (uint32_t)((((2 * ks + (c >> 1)) ^ r) << 4) + (c & 1) * 8);
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+              const uint2 b = lds64(xs + (uint32_t)(8 * nb + r) * 128 + koff);
+              mma_16816(acc[nb], a, b.x, b.y);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(ctrl->empty[s]));
+        if (++s == S) { s = 0; ph ^= 1u; }
+      }
+      if (!ok) break;
+
+      // ---- sum the two K-halves of each column group (fixed order: h0 + h1) ----
+      if (h == 1) {
+        if (seg > 0 && !wait_warp(bar(ctrl->red_free), (uint32_t)((seg - 1) & 1), wc)) break;
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+          for (int d = 0; d < 4; ++d) xchg[(nb * 4 + d) * 256 + g * 32 + lane] = acc[nb][d];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(ctrl->red_full));
+      } else {
+        if (!wait_warp(bar(ctrl->red_full), (uint32_t)(seg & 1), wc)) break;
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+          for (int d = 0; d < 4; ++d) acc[nb][d] += xchg[(nb * 4 + d) * 256 + g * 32 + lane];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(ctrl->red_free));
+
+        // ---- epilogue (even-half warps): fp16 Y, or fp32 partial + reduction ----
+        // accumulator d of block nb: column col_r + 8*(d >> 1), token 8nb + 2c + (d & 1)
+        const size_t y_col0 = (size_t)tile * kTileN + col_r;
+        if (whole) {
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int d = 0; d < 4; ++d) {
+              const int m = 8 * nb + 2 * c + (d & 1);
+              if (m < p.M)
+                p.Y[(size_t)m * p.N + y_col0 + 8 * (d >> 1)] =
+                    __half_as_ushort(__float2half_rn(acc[nb][d]));
+            }
+        } else {
+          const int slot = (tile == tile_begin) ? 0 : 1;
+          float* part = p.partials + ((size_t)blockIdx.x * 2 + slot) * ((size_t)p.bn * kTileN);
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int d = 0; d < 4; ++d) {
+              const int m = 8 * nb + 2 * c + (d & 1);
+              part[(size_t)m * kTileN + col_r + 8 * (d >> 1)] = acc[nb][d];
+            }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(ctrl->red_arrive));
+          const uint32_t rph = (uint32_t)(npartial & 1);
+          const long long c_first = stripe_owner((long long)tile * KT, U, G);
+          const long long c_last = stripe_owner((long long)tile * KT + KT - 1, U, G);
+          if (g == 0) {
+            if (!wait_warp(bar(ctrl->red_arrive), rph, wc)) break;
+            if (lane == 0) {
+              __threadfence();
+              const int expected = (int)(c_last - c_first + 1);
+              const int prev = atomicAdd(&p.counters[tile], 1);
+              const int last = (prev == expected - 1);
+              if (last) {
+                __threadfence();
+                p.counters[tile] = 0;
+              }
+              ctrl->reduce_last = last;
+              mbar_arrive(bar(ctrl->red_go));
+            }
+            __syncwarp();
+          }
+          if (!wait_warp(bar(ctrl->red_go), rph, wc)) break;
+          ++npartial;
+          if (*reinterpret_cast<volatile int*>(&ctrl->reduce_last)) {
+            // sum the contributors' partials in stripe order, 4 contributors per batch
+            float tot[NB][4];
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+              for (int d = 0; d < 4; ++d) tot[nb][d] = 0.f;
+            for (long long q0 = c_first; q0 <= c_last; q0 += 4) {
+              float v[4][NB][4];
+#pragma unroll
+              for (int jq = 0; jq < 4; ++jq) {
+                const long long q = q0 + jq;
+                if (q <= c_last) {
+                  const int qslot = ((long long)tile == stripe_begin(q, U, G) / KT) ? 0 : 1;
+                  const float* qp = p.partials + ((size_t)q * 2 + qslot) * ((size_t)p.bn * kTileN);
+#pragma unroll
+                  for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                    for (int d = 0; d < 4; ++d)
+                      v[jq][nb][d] = __ldcg(qp + (size_t)(8 * nb + 2 * c + (d & 1)) * kTileN + col_r +
+                                            8 * (d >> 1));
+                }
+              }
+#pragma unroll
+              for (int jq = 0; jq < 4; ++jq)
+                if (q0 + jq <= c_last) {
+#pragma unroll
+                  for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                    for (int d = 0; d < 4; ++d) tot[nb][d] += v[jq][nb][d];
+                }
+            }
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+              for (int d = 0; d < 4; ++d) {
+                const int m = 8 * nb + 2 * c + (d & 1);
+                if (m < p.M)
+                  p.Y[(size_t)m * p.N + y_col0 + 8 * (d >> 1)] =
+                      __half_as_ushort(__float2half_rn(tot[nb][d]));
+              }
+          }
+        }
+      }
+      ++seg;
+      u += seg_len;
+      ku = 0;
+      ++tile;
+    }
+  }
+  __syncwarp();
+  __syncthreads();
+}
+
+}  // namespace
+
+cudaError_t small_m_set_smem_limit(int bytes) {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(w4a16_small_m_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                bytes)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(w4a16_small_m_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                bytes)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(w4a16_small_m_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                bytes)) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(w4a16_small_m_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              bytes);
+}
+
+cudaError_t launch_small_m(const CUtensorMap& x_map, const GemmParams& p, int grid,
+                           uint32_t smem_bytes, cudaStream_t stream) {
+  switch (p.bn / 8) {
+    case 1: w4a16_small_m_kernel<1><<<grid, kSmThreads, smem_bytes, stream>>>(x_map, p); break;
+    case 2: w4a16_small_m_kernel<2><<<grid, kSmThreads, smem_bytes, stream>>>(x_map, p); break;
+    case 3: w4a16_small_m_kernel<3><<<grid, kSmThreads, smem_bytes, stream>>>(x_map, p); break;
+    case 4: w4a16_small_m_kernel<4><<<grid, kSmThreads, smem_bytes, stream>>>(x_map, p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace w4a16
