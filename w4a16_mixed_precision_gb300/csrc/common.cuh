@@ -86,6 +86,24 @@ __device__ __forceinline__ uint32_t as_u32(__half2 v) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// fp16x2 arithmetic on raw 32-bit registers, round to nearest even (explicit
+// rounding also keeps the compiler from fusing a multiply into an add).
+__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t f16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 // One 32-bit word of 8 codes -> the four fp16 pairs of a 16x16 operand
 // fragment: h[0] = column r, rows k..k+1; h[1] = column r+8, rows k..k+1;
 // h[2] = column r, rows k+2..k+3; h[3] = column r+8, rows k+2..k+3 (the
@@ -93,33 +111,34 @@ __device__ __forceinline__ uint32_t as_u32(__half2 v) {
 // ulp is 1 on [1024, 2048)); 0x6400 | (c << 4) is 1024 + 16c.  Subtracting
 // 1024 + z (or scaling by 1/16 and adding -(64 + z)) gives q - z exactly; the
 // single rounding of the dequantisation is the final multiply by the scale.
-__device__ __forceinline__ void dequant_frag(uint32_t w, __half2 sub_r, __half2 add_r8, __half2 s_r,
-                                             __half2 s_r8, uint32_t (&h)[4]) {
-  const __half2 sixteenth = as_h2(0x2C002C00u);
+// Arguments are fp16 pairs in 32-bit registers.
+__device__ __forceinline__ void dequant_frag(uint32_t w, uint32_t sub_r, uint32_t add_r8, uint32_t s_r,
+                                             uint32_t s_r8, uint32_t (&h)[4]) {
+  const uint32_t sixteenth = 0x2C002C00u;
   const uint32_t w8 = w >> 8;
   const uint32_t a = (w & 0x000F000Fu) | 0x64006400u;
   const uint32_t b = (w & 0x00F000F0u) | 0x64006400u;
   const uint32_t c = (w8 & 0x000F000Fu) | 0x64006400u;
   const uint32_t d = (w8 & 0x00F000F0u) | 0x64006400u;
-  h[0] = as_u32(__hmul2(__hsub2(as_h2(a), sub_r), s_r));
-  h[1] = as_u32(__hmul2(__hfma2(as_h2(b), sixteenth, add_r8), s_r8));
-  h[2] = as_u32(__hmul2(__hsub2(as_h2(c), sub_r), s_r));
-  h[3] = as_u32(__hmul2(__hfma2(as_h2(d), sixteenth, add_r8), s_r8));
+  h[0] = f16x2_mul(f16x2_sub(a, sub_r), s_r);
+  h[1] = f16x2_mul(f16x2_fma(b, sixteenth, add_r8), s_r8);
+  h[2] = f16x2_mul(f16x2_sub(c, sub_r), s_r);
+  h[3] = f16x2_mul(f16x2_fma(d, sixteenth, add_r8), s_r8);
 }
 
 // Per-column constants of the dequantisation: 1024 + z and -(64 + z) as fp16
 // pairs, and the scale broadcast to both halves.
 struct ColConst {
-  __half2 sub, add, s;
+  uint32_t sub, add, s;
 };
 
 __device__ __forceinline__ ColConst col_const(uint16_t s_bits, uint32_t z) {
   const uint32_t sub_u = 0x6400u | z;
   const uint32_t add_u = 0xD400u | (z << 4);
   ColConst k;
-  k.sub = as_h2(sub_u | (sub_u << 16));
-  k.add = as_h2(add_u | (add_u << 16));
-  k.s = as_h2((uint32_t)s_bits | ((uint32_t)s_bits << 16));
+  k.sub = sub_u | (sub_u << 16);
+  k.add = add_u | (add_u << 16);
+  k.s = (uint32_t)s_bits | ((uint32_t)s_bits << 16);
   return k;
 }
 

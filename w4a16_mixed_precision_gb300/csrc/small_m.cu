@@ -18,10 +18,10 @@
 //     unit) and warp 1 streams X (tensor copies, 128-byte swizzle) into a ring
 //     of mbarrier-guarded stages.
 //   * Warps 2..17: consumer warp (g, h) owns columns 16g..16g+15 of the tile
-//     and the 64-row chunks of parity h of every unit ("Marlin Project
-//     Overview", item "Warp Utilization": several warps compute partial results
-//     of one output tile); the two halves are summed through shared memory at
-//     the end of each tile.
+//     and half h (the first or last 64 or 128 rows) of every unit ("Marlin
+//     Project Overview", item "Warp Utilization": several warps compute partial
+//     results of one output tile); the two halves are summed through shared
+//     memory at the end of each tile.
 //   * The MMA's k order is permuted consistently for both operands: lane l
 //     holds rows 4(l%4)..4(l%4)+3 of every 16-row step (the repacked fragment
 //     order), so its X operand is one 8-byte shared load per step and token
@@ -64,7 +64,9 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   return v;
 }
 
-template <int NB>
+// NB: blocks of 8 tokens (M <= 8*NB).  JPW: 64-row chunks per consumer warp
+// per unit (a unit has 2*JPW chunks; warp half h takes chunks h*JPW .. +JPW-1).
+template <int NB, int JPW>
 __global__ void __launch_bounds__(kSmThreads, 1)
     w4a16_small_m_kernel(const __grid_constant__ CUtensorMap x_map, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -174,6 +176,18 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     const int c = lane & 3;
     const int col_r = 16 * g + r;  // this lane's two tile columns: col_r, col_r + 8
     const bool has_zeros = p.zeros != nullptr;
+    // X operand of k-step ks for token block nb: B column r reads token
+    // xr = sigma(r) = 2(r%4) + r/4 of the block (so the four rows a half-warp
+    // reads fall in four different 32-byte bank groups of the 128-byte
+    // swizzle), rows k = 16ks + 4c .. +3 = 16-byte unit 2ks + c/2, swizzled by xr.
+    const int xr = ((r & 3) << 1) | (r >> 2);
+    const uint32_t x_lane = (uint32_t)xr * 128 + (uint32_t)(c & 1) * 8;
+    uint32_t xoff[4];
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) xoff[ks] = (uint32_t)(((2 * ks + (c >> 1)) ^ xr) << 4);
+    // accumulator column 2c + e of a block is token sigma(2c + e)
+    const int tok0 = (((2 * c) & 3) << 1) | ((2 * c) >> 2);
+    const int tok1 = (((2 * c + 1) & 3) << 1) | ((2 * c + 1) >> 2);
     float acc[NB][4];
     int s = 0, seg = 0, npartial = 0;
     uint32_t ph = 0;
@@ -191,30 +205,33 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         if (!wait_warp(bar(ctrl->full[s]), ph, wc)) { ok = false; break; }
         const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
         const uint8_t* st_ptr = stage0_ptr + (size_t)s * p.stage_bytes;
-        for (int j = h; j < cpu; j += 2) {
-          const uint4 wv = lds128(st + p.off_codes + (uint32_t)j * kChunkCodeBytes +
-                                  (uint32_t)(g * 32 + lane) * 16);
-          const int gsub = (p.n_g > 1) ? (j >> 1) : 0;
-          const uint16_t* sc = reinterpret_cast<const uint16_t*>(st_ptr + p.off_scales) + gsub * kTileN;
-          uint32_t z0 = 8, z1 = 8;
-          if (has_zeros) {
-            const uint8_t* zb = st_ptr + p.off_zeros + gsub * (kTileN / 2);
-            z0 = (zb[col_r >> 1] >> ((col_r & 1) * 4)) & 0xFu;
-            z1 = (zb[(col_r + 8) >> 1] >> ((col_r & 1) * 4)) & 0xFu;
-          }
-          const ColConst k0 = col_const(sc[col_r], z0), k1 = col_const(sc[col_r + 8], z1);
-          const uint32_t xs = st + (uint32_t)j * p.x_chunk_bytes;
-          const uint32_t wk[4] = {wv.x, wv.y, wv.z, wv.w};
+        uint4 wv[JPW];
+#pragma unroll
+        for (int jj = 0; jj < JPW; ++jj)
+          wv[jj] = lds128(st + p.off_codes + (uint32_t)(h * JPW + jj) * kChunkCodeBytes +
+                          (uint32_t)(g * 32 + lane) * 16);
+        // this warp's chunks lie in one group row: row h of the unit when a unit
+        // spans two groups (group 128, 256-row units), else row 0
+        const int gsub = (p.n_g > 1) ? h : 0;
+        const uint16_t* sc = reinterpret_cast<const uint16_t*>(st_ptr + p.off_scales) + gsub * kTileN;
+        uint32_t z0 = 8, z1 = 8;
+        if (has_zeros) {
+          const uint8_t* zb = st_ptr + p.off_zeros + gsub * (kTileN / 2);
+          z0 = (zb[col_r >> 1] >> ((col_r & 1) * 4)) & 0xFu;
+          z1 = (zb[(col_r + 8) >> 1] >> ((col_r & 1) * 4)) & 0xFu;
+        }
+        const ColConst k0 = col_const(sc[col_r], z0), k1 = col_const(sc[col_r + 8], z1);
+#pragma unroll
+        for (int jj = 0; jj < JPW; ++jj) {
+          const uint32_t xs = st + (uint32_t)(h * JPW + jj) * p.x_chunk_bytes + x_lane;
+          const uint32_t wk[4] = {wv[jj].x, wv[jj].y, wv[jj].z, wv[jj].w};
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
             uint32_t a[4];
             dequant_frag(wk[ks], k0.sub, k1.add, k0.s, k1.s, a);
-            // X rows 8nb + r, k = 16ks + 4c .. +3: 16-byte chunk 2ks + c/2 of the
-            // 128-byte row, swizzled by the row index mod 8 (= r)
-            const uint32_t koff = (uint32_t)((((2 * ks + (c >> 1)) ^ r) << 4) + (c & 1) * 8);
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) {
-              const uint2 b = lds64(xs + (uint32_t)(8 * nb + r) * 128 + koff);
+              const uint2 b = lds64(xs + xoff[ks] + (uint32_t)nb * 1024);
               mma_16816(acc[nb], a, b.x, b.y);
             }
           }
@@ -244,14 +261,14 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         if (lane == 0) mbar_arrive(bar(ctrl->red_free));
 
         // ---- epilogue (even-half warps): fp16 Y, or fp32 partial + reduction ----
-        // accumulator d of block nb: column col_r + 8*(d >> 1), token 8nb + 2c + (d & 1)
+        // accumulator d of block nb: column col_r + 8*(d >> 1), token 8nb + tok[d & 1]
         const size_t y_col0 = (size_t)tile * kTileN + col_r;
         if (whole) {
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
             for (int d = 0; d < 4; ++d) {
-              const int m = 8 * nb + 2 * c + (d & 1);
+              const int m = 8 * nb + ((d & 1) ? tok1 : tok0);
               if (m < p.M)
                 p.Y[(size_t)m * p.N + y_col0 + 8 * (d >> 1)] =
                     __half_as_ushort(__float2half_rn(acc[nb][d]));
@@ -263,7 +280,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
           for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
             for (int d = 0; d < 4; ++d) {
-              const int m = 8 * nb + 2 * c + (d & 1);
+              const int m = 8 * nb + ((d & 1) ? tok1 : tok0);
               part[(size_t)m * kTileN + col_r + 8 * (d >> 1)] = acc[nb][d];
             }
           __syncwarp();
@@ -308,7 +325,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
                   for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
                     for (int d = 0; d < 4; ++d)
-                      v[jq][nb][d] = __ldcg(qp + (size_t)(8 * nb + 2 * c + (d & 1)) * kTileN + col_r +
+                      v[jq][nb][d] = __ldcg(qp + (size_t)(8 * nb + ((d & 1) ? tok1 : tok0)) * kTileN + col_r +
                                             8 * (d >> 1));
                 }
               }
@@ -325,7 +342,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
             for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
               for (int d = 0; d < 4; ++d) {
-                const int m = 8 * nb + 2 * c + (d & 1);
+                const int m = 8 * nb + ((d & 1) ? tok1 : tok0);
                 if (m < p.M)
                   p.Y[(size_t)m * p.N + y_col0 + 8 * (d >> 1)] =
                       __half_as_ushort(__float2half_rn(tot[nb][d]));
@@ -345,31 +362,30 @@ __global__ void __launch_bounds__(kSmThreads, 1)
 
 }  // namespace
 
+#define W4A16_SMALL_M_KERNELS(X) X(1, 1) X(2, 1) X(3, 1) X(4, 1) X(1, 2) X(2, 2) X(3, 2) X(4, 2)
+
 cudaError_t small_m_set_smem_limit(int bytes) {
-  cudaError_t e;
-  if ((e = cudaFuncSetAttribute(w4a16_small_m_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                bytes)) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(w4a16_small_m_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                bytes)) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(w4a16_small_m_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                bytes)) != cudaSuccess)
-    return e;
-  return cudaFuncSetAttribute(w4a16_small_m_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              bytes);
+  cudaError_t e = cudaSuccess;
+#define W4A16_SET(NB, JPW)                                                                   \
+  if (e == cudaSuccess)                                                                      \
+    e = cudaFuncSetAttribute(w4a16_small_m_kernel<NB, JPW>,                                  \
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  W4A16_SMALL_M_KERNELS(W4A16_SET)
+#undef W4A16_SET
+  return e;
 }
 
 cudaError_t launch_small_m(const CUtensorMap& x_map, const GemmParams& p, int grid,
                            uint32_t smem_bytes, cudaStream_t stream) {
-  switch (p.bn / 8) {
-    case 1: w4a16_small_m_kernel<1><<<grid, kSmThreads, smem_bytes, stream>>>(x_map, p); break;
-    case 2: w4a16_small_m_kernel<2><<<grid, kSmThreads, smem_bytes, stream>>>(x_map, p); break;
-    case 3: w4a16_small_m_kernel<3><<<grid, kSmThreads, smem_bytes, stream>>>(x_map, p); break;
-    case 4: w4a16_small_m_kernel<4><<<grid, kSmThreads, smem_bytes, stream>>>(x_map, p); break;
-    default: return cudaErrorInvalidValue;
+  const int nb = p.bn / 8, jpw = p.cpu / 2;
+#define W4A16_LAUNCH(NB, JPW)                                                                  \
+  if (nb == NB && jpw == JPW) {                                                                \
+    w4a16_small_m_kernel<NB, JPW><<<grid, kSmThreads, smem_bytes, stream>>>(x_map, p);         \
+    return cudaGetLastError();                                                                 \
   }
-  return cudaGetLastError();
+  W4A16_SMALL_M_KERNELS(W4A16_LAUNCH)
+#undef W4A16_LAUNCH
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace w4a16
