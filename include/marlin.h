@@ -132,6 +132,36 @@ marlin_status_t marlin_gemm(const uint16_t* X, const void* packed, const uint16_
                             void* workspace, size_t workspace_bytes, marlin_stream_t stream);
 
 /*
+ * marlin_gemm without a caller-provided workspace.  The Marlin pages have no
+ * counterpart to this entry point.
+ *
+ * For callers that cannot allocate device memory: an operator embedded in a
+ * host framework whose memory planner owns all device memory and hands the
+ * operator only its inputs and outputs, or code on a latency-critical path
+ * where the implicit device synchronisation of cudaMalloc/cudaFree is not
+ * acceptable.  The scratch that marlin_gemm keeps in `workspace` lives here in
+ * a static device array of the library (8 MiB, held by every GPU that loads
+ * the library until the process exits).  This call allocates nothing.
+ *
+ * Arguments as for marlin_gemm, without workspace.  Results are identical to
+ * marlin_gemm's for the same inputs.
+ * Limit: problems whose marlin_workspace_bytes exceeds 8 MiB (on a 152-SM
+ * GB300, M > 48) return MARLIN_ERR_WORKSPACE_TOO_SMALL before anything is
+ * launched; other argument errors as for marlin_gemm.
+ * Set-up: the first call on a device looks up the array's device address
+ * (once per device, with that device current); make that first call before
+ * any stream capture.  Each call clears the status word and tile counters on
+ * `stream` before launching.
+ * All calls share one array: calls that overlap on the GPU (different
+ * streams, or different host threads on one device without ordering) race and
+ * give wrong results.  A bounded wait that expires inside the kernel is
+ * recorded only in the library's array and is not reported.
+ */
+marlin_status_t marlin_gemm_no_alloc(const uint16_t* X, const void* packed, const uint16_t* scales,
+                                     const int32_t* zeros, uint16_t* Y, int M, int K, int N,
+                                     int group, marlin_stream_t stream);
+
+/*
  * Synchronises `stream`, reads and clears the device status word that
  * marlin_gemm keeps in `workspace`, and returns MARLIN_OK or
  * MARLIN_ERR_TIMEOUT (a bounded wait in a kernel expired; that call's Y is

@@ -29,6 +29,7 @@ EXPORTS = (
     "marlin_repack",
     "marlin_workspace_bytes",
     "marlin_gemm",
+    "marlin_gemm_no_alloc",
     "marlin_last_device_status",
 )
 
@@ -63,6 +64,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.marlin_workspace_bytes.argtypes = [I, I, I, I, I, ctypes.POINTER(SZ)]
         lib.marlin_gemm.argtypes = [P, P, P, P, P, I, I, I, I, P, SZ, P]
         lib.marlin_last_device_status.argtypes = [P, P]
+        lib.marlin_gemm_no_alloc.argtypes = [P, P, P, P, P, I, I, I, I, P]
+        lib.marlin_gemm_no_alloc.restype = I
         for f in ("marlin_packed_layout", "marlin_repack", "marlin_workspace_bytes", "marlin_gemm",
                   "marlin_last_device_status"):
             getattr(lib, f).restype = I
@@ -106,6 +109,14 @@ def gemm_raw(x_ptr: int, packed_ptr: int, scales_ptr: int, zeros_ptr: int | None
     """Raw call; returns the status code."""
     return load().marlin_gemm(x_ptr, packed_ptr, scales_ptr, zeros_ptr or None, y_ptr, M, K, N,
                               group, ws_ptr, ws_bytes, stream or None)
+
+
+def gemm_no_alloc_raw(x_ptr: int, packed_ptr: int, scales_ptr: int, zeros_ptr: int | None, y_ptr: int,
+                     M: int, K: int, N: int, group: int, stream: int) -> int:
+    """Raw call of the entry point that uses the library's own scratch
+    (for callers that cannot allocate a workspace); returns the status code."""
+    return load().marlin_gemm_no_alloc(x_ptr, packed_ptr, scales_ptr, zeros_ptr or None, y_ptr, M, K,
+                                       N, group, stream or None)
 
 
 def last_device_status(ws_ptr: int, stream: int) -> int:
