@@ -112,6 +112,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctrl->tmem_base;
+  // Programmatic dependent launch: the next kernel in the stream may be
+  // scheduled as soon as SMs free up, and this one waits here, after its
+  // prologue, until the previous kernel has finished and its writes are
+  // visible -- so launch latency and set-up overlap the previous kernel.
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  griddep_wait();
 
   if (warp == 0) {
     // ================= producer: TMA into the stage ring =================
@@ -401,8 +407,17 @@ cudaError_t gemm_set_smem_limit(int bytes) {
 
 cudaError_t launch_gemm(const CUtensorMap& x_map, const GemmParams& p, int grid, uint32_t smem_bytes,
                         cudaStream_t stream) {
-  w4a16_gemm_kernel<<<grid, kThreads, smem_bytes, stream>>>(x_map, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, w4a16_gemm_kernel, x_map, p);
 }
 
 }  // namespace w4a16

@@ -194,6 +194,19 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
+// ---- programmatic dependent launch -------------------------------------------------
+
+// Block until every grid this launch depends on has completed and its memory
+// operations are visible (no-op when the launch has no such dependency).
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next kernel in the stream to be scheduled before this one ends.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- named barrier over a subset of warps ----------------------------------------------
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {

@@ -108,6 +108,12 @@ __global__ void __launch_bounds__(kSmThreads, 1)
   if (warp == 1 && lane == 0) prefetch_tensormap(&x_map);
   __syncthreads();
   const WaitCtx wc{&ctrl->abort, p.status, p.timeout_ns};
+  // Programmatic dependent launch: the next kernel in the stream may be
+  // scheduled as soon as SMs free up, and this one waits here, after its
+  // prologue, until the previous kernel has finished and its writes are
+  // visible -- so launch latency and set-up overlap the previous kernel.
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  griddep_wait();
 
   if (warp == 0) {
     // ================= weights producer =================
@@ -378,11 +384,18 @@ cudaError_t small_m_set_smem_limit(int bytes) {
 cudaError_t launch_small_m(const CUtensorMap& x_map, const GemmParams& p, int grid,
                            uint32_t smem_bytes, cudaStream_t stream) {
   const int nb = p.bn / 8, jpw = p.cpu / 2;
-#define W4A16_LAUNCH(NB, JPW)                                                                  \
-  if (nb == NB && jpw == JPW) {                                                                \
-    w4a16_small_m_kernel<NB, JPW><<<grid, kSmThreads, smem_bytes, stream>>>(x_map, p);         \
-    return cudaGetLastError();                                                                 \
-  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kSmThreads);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+#define W4A16_LAUNCH(NB, JPW) \
+  if (nb == NB && jpw == JPW) return cudaLaunchKernelEx(&cfg, w4a16_small_m_kernel<NB, JPW>, x_map, p);
   W4A16_SMALL_M_KERNELS(W4A16_LAUNCH)
 #undef W4A16_LAUNCH
   return cudaErrorInvalidValue;
