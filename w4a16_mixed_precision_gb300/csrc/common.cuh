@@ -77,6 +77,46 @@ __device__ __forceinline__ long long stripe_owner(long long u, long long U, long
   return ((u + 1) * G - 1) / U;
 }
 
+// ---- split-tile reduction across CTAs ----------------------------------------------
+// A column tile cut by stripe boundaries is finished by its reducer: the CTA
+// that owns the tile's first unit.  For that CTA the tile is always its last
+// segment (its stripe ends inside the tile), and for every other contributor
+// the tile is its first segment (its stripe starts inside the tile).  So each
+// CTA publishes at most one partial tile (from its first segment, then goes on
+// without waiting) and reduces at most one (at its very end), and no CTA ever
+// waits for a CTA that is itself waiting: the wait graph has no cycles.
+
+__device__ __forceinline__ long long tile_reducer(long long tile, long long KT, long long U,
+                                                  long long G) {
+  return stripe_owner(tile * KT, U, G);
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded spin until *counter reaches `expected` (acquire).  Returns false on
+// timeout (recorded in the status word) or when the CTA is aborting.
+static __device__ __noinline__ bool wait_counter(const int* counter, int expected, const WaitCtx& c) {
+  const uint64_t t0 = global_timer_ns();
+#pragma unroll 1
+  while (ld_acquire_gpu(counter) < expected) {
+    if (*reinterpret_cast<volatile int*>(c.abort)) return false;
+    if (global_timer_ns() - t0 > c.timeout_ns) {
+      raise_timeout(c);
+      return false;
+    }
+    __nanosleep(100);
+  }
+  return true;
+}
+
 // ---- dequantisation -------------------------------------------------------------
 
 __device__ __forceinline__ __half2 as_h2(uint32_t v) {

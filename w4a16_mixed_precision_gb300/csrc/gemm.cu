@@ -11,8 +11,8 @@
 //   * One persistent CTA per SM walks a contiguous stripe of work units
 //     (m-tile, n-tile, K-slice) -- the pages' "striped partitioning"
 //     ("Marlin Project Overview", section "Key Techniques").  Column tiles cut by
-//     a stripe boundary are summed through an fp32 workspace by the last CTA to
-//     arrive, in a fixed order, so results are bit-reproducible.
+//     a stripe boundary are summed through an fp32 workspace by the CTA owning
+//     the tile's first unit, in a fixed order, so results are bit-reproducible.
 //   * Warp roles: warp 0 streams packed codes, scales, zeros (bulk TMA) and X
 //     (tensor TMA, 128-byte swizzle) through a multi-stage mbarrier ring in shared
 //     memory ("Marlin", section "async copy and pipeline"); warps 4..11 (two
@@ -41,11 +41,10 @@ struct Ctrl {
   uint64_t dfull;
   uint64_t dempty;
   uint64_t drain;
-  uint64_t red_arrive;  // dequant warps -> reducer leader: partial tile stored
-  uint64_t red_go;      // leader -> dequant warps: arrival counted
+  uint64_t red_arrive;  // dequant warps -> leader: partial tile stored (contributor)
+  uint64_t red_go;      // leader -> dequant warps: all partials published (reducer)
   uint32_t tmem_base;
   int abort;
-  int reduce_last;
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
 
@@ -100,7 +99,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(ctrl->red_arrive), kNumDqWarps);
     mbar_init(bar(ctrl->red_go), 1);
     ctrl->abort = 0;
-    ctrl->reduce_last = 0;
     fence_mbarrier_init();
     prefetch_tensormap(&x_map);
   }
@@ -219,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // dequantisation: this thread holds fragment lane `lane` of the two 16-column
     // groups 2*quarter and 2*quarter+1, i.e. columns fr + {0, 8} of each
     const int fr = lane >> 2;
-    int s = 0, a = 0, ch = 0, seg = 0, npartial = 0;
+    int s = 0, a = 0, ch = 0, seg = 0;
     uint32_t ph = 0, aph = 0;
     int u = u_begin, ku = ku_begin, tile = tile_begin;
     bool ok = true;
@@ -294,23 +292,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait_warp(bar(ctrl->dfull), (uint32_t)(seg & 1), wc)) break;
       tc_fence_after();
       const bool whole = (ku == 0 && seg_len == KT);
-      const int slot = (tile == tile_begin) ? 0 : 1;
-      float* part = p.partials + ((size_t)blockIdx.x * 2 + slot) * ((size_t)p.bn * kTileN);
       const int m_base = mt * p.bn;
       const size_t y_col = (size_t)nt * kTileN + row;
+      const long long c_first = tile_reducer(tile, KT, U, G);
+      const long long c_last = stripe_owner((long long)tile * KT + KT - 1, U, G);
+      const bool reducer = !whole && (long long)blockIdx.x == c_first;
+      if (reducer) {
+        // reducer (this is its last segment): wait until the other
+        // contributors have published their partial tiles
+        if (dq == 0) {
+          if (lane == 0) {
+            if (wait_counter(&p.counters[tile], (int)(c_last - c_first), wc))
+              p.counters[tile] = 0;  // leave the workspace zeroed for the next call
+            mbar_arrive(bar(ctrl->red_go));
+          }
+          __syncwarp();
+        }
+        if (!wait_warp(bar(ctrl->red_go), 0, wc)) break;
+        if (*reinterpret_cast<volatile int*>(&ctrl->abort)) break;
+      }
+      float* part = p.partials + (size_t)blockIdx.x * ((size_t)p.bn * kTileN);
       for (int cc = wg; cc < p.bn / 8; cc += 2) {
         uint32_t r[8];
         tmem_ld_x8(tmem + lane_off + (uint32_t)cc * 8, r);
         tmem_wait_ld();
+        float acc[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[c] = __uint_as_float(r[c]);
+        if (reducer) {
+          // own partial first, then the others' in stripe order (fixed order,
+          // bit-reproducible); loads of 4 contributors are issued together
+          for (long long q0 = c_first + 1; q0 <= c_last; q0 += 4) {
+            float v[4][8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if (q0 + j <= c_last) {
+                const float* qp = p.partials + (size_t)(q0 + j) * ((size_t)p.bn * kTileN) +
+                                  (size_t)(cc * 8) * kTileN + row;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) v[j][c] = __ldcg(qp + (size_t)c * kTileN);
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (q0 + j <= c_last) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) acc[c] += v[j][c];
+              }
+          }
+        }
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const int m = cc * 8 + c;
-          const float f = __uint_as_float(r[c]);
-          if (whole) {
+          if (whole || reducer) {
             if (m_base + m < p.M)
-              p.Y[(size_t)(m_base + m) * p.N + y_col] = __half_as_ushort(__float2half_rn(f));
+              p.Y[(size_t)(m_base + m) * p.N + y_col] = __half_as_ushort(__float2half_rn(acc[c]));
           } else {
-            part[(size_t)m * kTileN + row] = f;
+            part[(size_t)m * kTileN + row] = acc[c];
           }
         }
       }
@@ -318,68 +356,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(ctrl->dempty));
 
-      if (!whole) {
-        // ---- global reduction: the last CTA to store its partial sums the tile ----
-        // The warps' partial stores are ordered before the leader's arrival
-        // count by the CTA-scoped mbarrier and the leader's gpu-scoped fence.
+      if (!whole && !reducer) {
+        // contributor (this is its first segment): publish the partial tile
+        // with one release increment and go on.  The warps' stores are ordered
+        // before it by the CTA-scoped mbarrier and the leader's gpu fence.
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(ctrl->red_arrive));
-        const uint32_t rph = (uint32_t)(npartial & 1);
-        const long long c_first = stripe_owner((long long)tile * KT, U, G);
-        const long long c_last = stripe_owner((long long)tile * KT + KT - 1, U, G);
         if (dq == 0) {
-          if (!wait_warp(bar(ctrl->red_arrive), rph, wc)) break;
+          if (!wait_warp(bar(ctrl->red_arrive), 0, wc)) break;
           if (lane == 0) {
             __threadfence();
-            const int expected = (int)(c_last - c_first + 1);
-            const int prev = atomicAdd(&p.counters[tile], 1);
-            const int last = (prev == expected - 1);
-            if (last) {
-              __threadfence();
-              p.counters[tile] = 0;  // leave the workspace zeroed for the next call
-            }
-            ctrl->reduce_last = last;
-            mbar_arrive(bar(ctrl->red_go));
+            red_release_gpu_add(&p.counters[tile], 1);
           }
           __syncwarp();
-        }
-        if (!wait_warp(bar(ctrl->red_go), rph, wc)) break;
-        ++npartial;
-        if (*reinterpret_cast<volatile int*>(&ctrl->reduce_last)) {
-          // Sum the contributors' partial tiles in stripe order (fixed, so the
-          // result is bit-reproducible).  Loads of 4 contributors x 8 columns
-          // are issued together to overlap their L2 latency.
-          for (int cc = wg; cc < p.bn / 8; cc += 2) {
-            float acc[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) acc[c] = 0.f;
-            for (long long q0 = c_first; q0 <= c_last; q0 += 4) {
-              float v[4][8];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const long long q = q0 + j;
-                if (q <= c_last) {
-                  const int qslot = ((long long)tile == stripe_begin(q, U, G) / KT) ? 0 : 1;
-                  const float* qp = p.partials + ((size_t)q * 2 + qslot) * ((size_t)p.bn * kTileN) +
-                                    (size_t)(cc * 8) * kTileN + row;
-#pragma unroll
-                  for (int c = 0; c < 8; ++c) v[j][c] = __ldcg(qp + (size_t)c * kTileN);
-                }
-              }
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                if (q0 + j <= c_last) {
-#pragma unroll
-                  for (int c = 0; c < 8; ++c) acc[c] += v[j][c];
-                }
-            }
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const int m = cc * 8 + c;
-              if (m_base + m < p.M)
-                p.Y[(size_t)(m_base + m) * p.N + y_col] = __half_as_ushort(__float2half_rn(acc[c]));
-            }
-          }
         }
       }
       ++seg;

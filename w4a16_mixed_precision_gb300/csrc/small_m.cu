@@ -13,7 +13,7 @@
 //   * One persistent CTA per SM takes an equal stripe of (128-column tile,
 //     K-slice) units ("Marlin Project Overview", section "Key Techniques",
 //     item "Striped Partitioning"); tiles cut by a stripe boundary are summed by
-//     the last CTA to store its fp32 partial, in a fixed order.
+//     the CTA that owns the tile's first unit, in a fixed order.
 //   * Warp 0 streams the weights (codes, scales, zeros: one bulk copy each per
 //     unit) and warp 1 streams X (tensor copies, 128-byte swizzle) into a ring
 //     of mbarrier-guarded stages.
@@ -42,10 +42,9 @@ struct SmCtrl {
   uint64_t empty[kMaxStages];
   uint64_t red_full;    // odd-half warps -> even-half warps: accumulators in smem
   uint64_t red_free;    // even-half warps -> odd-half warps: exchange buffer read
-  uint64_t red_arrive;  // even-half warps -> leader: partial tile stored
-  uint64_t red_go;      // leader -> even-half warps: arrival counted
+  uint64_t red_arrive;  // even-half warps -> leader: partial tile stored (contributor)
+  uint64_t red_go;      // leader -> even-half warps: all partials published (reducer)
   int abort;
-  int reduce_last;
 };
 static_assert(sizeof(SmCtrl) <= kCtrlBytes, "control block too large");
 
@@ -102,7 +101,6 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     mbar_init(bar(ctrl->red_arrive), kSmConsumers / 2);
     mbar_init(bar(ctrl->red_go), 1);
     ctrl->abort = 0;
-    ctrl->reduce_last = 0;
     fence_mbarrier_init();
   }
   if (warp == 1 && lane == 0) prefetch_tensormap(&x_map);
@@ -195,7 +193,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     const int tok0 = (((2 * c) & 3) << 1) | ((2 * c) >> 2);
     const int tok1 = (((2 * c + 1) & 3) << 1) | ((2 * c + 1) >> 2);
     float acc[NB][4];
-    int s = 0, seg = 0, npartial = 0;
+    int s = 0, seg = 0;
     uint32_t ph = 0;
     int u = u_begin, ku = ku_begin, tile = tile_begin;
     bool ok = true;
@@ -280,79 +278,72 @@ __global__ void __launch_bounds__(kSmThreads, 1)
                     __half_as_ushort(__float2half_rn(acc[nb][d]));
             }
         } else {
-          const int slot = (tile == tile_begin) ? 0 : 1;
-          float* part = p.partials + ((size_t)blockIdx.x * 2 + slot) * ((size_t)p.bn * kTileN);
-#pragma unroll
-          for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-            for (int d = 0; d < 4; ++d) {
-              const int m = 8 * nb + ((d & 1) ? tok1 : tok0);
-              part[(size_t)m * kTileN + col_r + 8 * (d >> 1)] = acc[nb][d];
-            }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(ctrl->red_arrive));
-          const uint32_t rph = (uint32_t)(npartial & 1);
-          const long long c_first = stripe_owner((long long)tile * KT, U, G);
+          const long long c_first = tile_reducer(tile, KT, U, G);
           const long long c_last = stripe_owner((long long)tile * KT + KT - 1, U, G);
-          if (g == 0) {
-            if (!wait_warp(bar(ctrl->red_arrive), rph, wc)) break;
-            if (lane == 0) {
-              __threadfence();
-              const int expected = (int)(c_last - c_first + 1);
-              const int prev = atomicAdd(&p.counters[tile], 1);
-              const int last = (prev == expected - 1);
-              if (last) {
-                __threadfence();
-                p.counters[tile] = 0;
-              }
-              ctrl->reduce_last = last;
-              mbar_arrive(bar(ctrl->red_go));
-            }
-            __syncwarp();
-          }
-          if (!wait_warp(bar(ctrl->red_go), rph, wc)) break;
-          ++npartial;
-          if (*reinterpret_cast<volatile int*>(&ctrl->reduce_last)) {
-            // sum the contributors' partials in stripe order, 4 contributors per batch
-            float tot[NB][4];
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-              for (int d = 0; d < 4; ++d) tot[nb][d] = 0.f;
-            for (long long q0 = c_first; q0 <= c_last; q0 += 4) {
-              float v[4][NB][4];
-#pragma unroll
-              for (int jq = 0; jq < 4; ++jq) {
-                const long long q = q0 + jq;
-                if (q <= c_last) {
-                  const int qslot = ((long long)tile == stripe_begin(q, U, G) / KT) ? 0 : 1;
-                  const float* qp = p.partials + ((size_t)q * 2 + qslot) * ((size_t)p.bn * kTileN);
-#pragma unroll
-                  for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-                    for (int d = 0; d < 4; ++d)
-                      v[jq][nb][d] = __ldcg(qp + (size_t)(8 * nb + ((d & 1) ? tok1 : tok0)) * kTileN + col_r +
-                                            8 * (d >> 1));
-                }
-              }
-#pragma unroll
-              for (int jq = 0; jq < 4; ++jq)
-                if (q0 + jq <= c_last) {
-#pragma unroll
-                  for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-                    for (int d = 0; d < 4; ++d) tot[nb][d] += v[jq][nb][d];
-                }
-            }
+          if ((long long)blockIdx.x != c_first) {
+            // contributor (this is its first segment): store the partial tile,
+            // publish it with one release increment, and go on
+            float* part = p.partials + (size_t)blockIdx.x * ((size_t)p.bn * kTileN);
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
               for (int d = 0; d < 4; ++d) {
                 const int m = 8 * nb + ((d & 1) ? tok1 : tok0);
+                part[(size_t)m * kTileN + col_r + 8 * (d >> 1)] = acc[nb][d];
+              }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(ctrl->red_arrive));
+            if (g == 0) {
+              if (!wait_warp(bar(ctrl->red_arrive), 0, wc)) break;
+              if (lane == 0) {
+                __threadfence();
+                red_release_gpu_add(&p.counters[tile], 1);
+              }
+              __syncwarp();
+            }
+          } else {
+            // reducer (this is its last segment): wait for the other
+            // contributors, then sum in stripe order -- own partial first
+            if (g == 0) {
+              if (lane == 0) {
+                if (wait_counter(&p.counters[tile], (int)(c_last - c_first), wc))
+                  p.counters[tile] = 0;  // leave the workspace zeroed for the next call
+                mbar_arrive(bar(ctrl->red_go));
+              }
+              __syncwarp();
+            }
+            if (!wait_warp(bar(ctrl->red_go), 0, wc)) break;
+            if (*reinterpret_cast<volatile int*>(&ctrl->abort)) break;
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+              float tot[4] = {acc[nb][0], acc[nb][1], acc[nb][2], acc[nb][3]};
+              for (long long q0 = c_first + 1; q0 <= c_last; q0 += 4) {
+                float v[4][4];
+#pragma unroll
+                for (int jq = 0; jq < 4; ++jq) {
+                  if (q0 + jq <= c_last) {
+                    const float* qp = p.partials + (size_t)(q0 + jq) * ((size_t)p.bn * kTileN);
+#pragma unroll
+                    for (int d = 0; d < 4; ++d)
+                      v[jq][d] = __ldcg(qp + (size_t)(8 * nb + ((d & 1) ? tok1 : tok0)) * kTileN +
+                                        col_r + 8 * (d >> 1));
+                  }
+                }
+#pragma unroll
+                for (int jq = 0; jq < 4; ++jq)
+                  if (q0 + jq <= c_last) {
+#pragma unroll
+                    for (int d = 0; d < 4; ++d) tot[d] += v[jq][d];
+                  }
+              }
+#pragma unroll
+              for (int d = 0; d < 4; ++d) {
+                const int m = 8 * nb + ((d & 1) ? tok1 : tok0);
                 if (m < p.M)
                   p.Y[(size_t)m * p.N + y_col0 + 8 * (d >> 1)] =
-                      __half_as_ushort(__float2half_rn(tot[nb][d]));
+                      __half_as_ushort(__float2half_rn(tot[d]));
               }
+            }
           }
         }
       }
