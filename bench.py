@@ -435,7 +435,7 @@ def run_gpu(args, problems, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
-def per_run_table(problems, packed, ws, xs, ys, dev, peaks, reps=60):
+def per_run_table(problems, packed, ws, xs, ys, dev, peaks):
     import torch
 
     import w4a16_mixed_precision_gb300 as w4
@@ -450,30 +450,36 @@ def per_run_table(problems, packed, ws, xs, ys, dev, peaks, reps=60):
             n = max(2, min(len(packed[lk]), -(-2 * L2_BYTES // (p.K * p.N * 2)) + 1))
             fp16_w[lk] = [torch.randn((p.K, p.N), dtype=torch.float16, device=dev, generator=g)
                           for _ in range(n)]
+    stream = torch.cuda.Stream()
     for i, p in enumerate(problems):
         lk = (p.K, p.N, p.group, p.asym)
         R = len(packed[lk])
         Rf = len(fp16_w[lk])
-        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        for _ in range(3):
-            w4.gemm_into(xs[i], packed[lk][0], ws[lk], ys[i])
-        torch.cuda.synchronize()
-        s0.record()
-        for r in range(reps):
-            w4.gemm_into(xs[i], packed[lk][r % R], ws[lk], ys[i])
-        s1.record()
-        torch.cuda.synchronize()
-        us = s0.elapsed_time(s1) * 1e3 / reps
-        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        for _ in range(3):
-            torch.matmul(xs[i], fp16_w[lk][0])
-        torch.cuda.synchronize()
-        c0.record()
-        for r in range(reps):
-            torch.matmul(xs[i], fp16_w[lk][r % Rf])
-        c1.record()
-        torch.cuda.synchronize()
-        cu = c0.elapsed_time(c1) * 1e3 / reps
+        reps = 60 if p.M * p.N * 2 < (64 << 20) else 6   # bounds the graphs' output memory
+        # both sides captured as CUDA graphs of `reps` launches over rotating
+        # copies, so host launch cost does not enter the per-call time
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                w4.gemm_into(xs[i], packed[lk][0], ws[lk], ys[i])
+                torch.matmul(xs[i], fp16_w[lk][0])
+            stream.synchronize()
+            g_ours, g_ref = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_ours, stream=stream):
+                for r in range(reps):
+                    w4.gemm_into(xs[i], packed[lk][r % R], ws[lk], ys[i])
+            with torch.cuda.graph(g_ref, stream=stream):
+                for r in range(reps):
+                    torch.matmul(xs[i], fp16_w[lk][r % Rf])
+            times = []
+            for g in (g_ours, g_ref):
+                g.replay()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                stream.synchronize()
+                times.append(e0.elapsed_time(e1) * 1e3 / reps)
+        us, cu = times
         gbs = p.algorithmic_bytes() / (us * 1e-6) / 1e9
         tfl = p.flops() / (us * 1e-6) / 1e12
         out.append({"M": p.M, "K": p.K, "N": p.N, "group": p.group, "zeros": p.asym, "us": round(us, 3),

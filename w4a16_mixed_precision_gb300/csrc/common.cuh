@@ -166,6 +166,74 @@ __device__ __forceinline__ void dequant_frag(uint32_t w, uint32_t sub_r, uint32_
   h[3] = f16x2_mul(f16x2_fma(d, sixteenth, add_r8), s_r8);
 }
 
+// The same dequantisation fused with the tensor-core multiply-accumulates that
+// consume it, as one block of PTX: the four fp16 pairs are produced directly in
+// the registers the mma.sync A operand reads (written as separate statements,
+// the compiler surrounds them with register moves).  NB mma.sync.m16n8k16 share
+// the A fragment, one per block of 8 tokens: acc[nb] += A * B[nb].
+#define W4A16_DEQ_PTX(W, SUB, ADD, S, S8)                                 \
+  ".reg .b32 t0, t1, t2, t3, w8, k16;\n\t"                                \
+  "mov.b32 k16, 0x2C002C00;\n\t"                                         \
+  "lop3.b32 t0, " W ", 0x000F000F, 0x64006400, 0xEA;\n\t"                \
+  "lop3.b32 t1, " W ", 0x00F000F0, 0x64006400, 0xEA;\n\t"                \
+  "shr.u32 w8, " W ", 8;\n\t"                                             \
+  "lop3.b32 t2, w8, 0x000F000F, 0x64006400, 0xEA;\n\t"                    \
+  "lop3.b32 t3, w8, 0x00F000F0, 0x64006400, 0xEA;\n\t"                    \
+  "sub.rn.f16x2 t0, t0, " SUB ";\n\t"                                     \
+  "fma.rn.f16x2 t1, t1, k16, " ADD ";\n\t"                                \
+  "sub.rn.f16x2 t2, t2, " SUB ";\n\t"                                     \
+  "fma.rn.f16x2 t3, t3, k16, " ADD ";\n\t"                                \
+  "mul.rn.f16x2 t0, t0, " S ";\n\t"                                       \
+  "mul.rn.f16x2 t1, t1, " S8 ";\n\t"                                      \
+  "mul.rn.f16x2 t2, t2, " S ";\n\t"                                       \
+  "mul.rn.f16x2 t3, t3, " S8 ";\n\t"
+#define W4A16_MMA_PTX(D0, D1, D2, D3, B0, B1)                                                     \
+  "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {" D0 ", " D1 ", " D2 ", " D3 "}, "           \
+  "{t0, t1, t2, t3}, {" B0 ", " B1 "}, {" D0 ", " D1 ", " D2 ", " D3 "};\n\t"
+
+template <int NB>
+__device__ __forceinline__ void dequant_mma(float (&acc)[NB][4], uint32_t w, uint32_t sub_r,
+                                            uint32_t add_r8, uint32_t s_r, uint32_t s_r8,
+                                            const uint2 (&b)[NB]) {
+  if constexpr (NB == 1) {
+    asm volatile("{\n\t" W4A16_DEQ_PTX("%4", "%5", "%6", "%7", "%8")
+                 W4A16_MMA_PTX("%0", "%1", "%2", "%3", "%9", "%10") "}"
+                 : "+f"(acc[0][0]), "+f"(acc[0][1]), "+f"(acc[0][2]), "+f"(acc[0][3])
+                 : "r"(w), "r"(sub_r), "r"(add_r8), "r"(s_r), "r"(s_r8), "r"(b[0].x), "r"(b[0].y));
+  } else if constexpr (NB == 2) {
+    asm volatile("{\n\t" W4A16_DEQ_PTX("%8", "%9", "%10", "%11", "%12")
+                 W4A16_MMA_PTX("%0", "%1", "%2", "%3", "%13", "%14")
+                 W4A16_MMA_PTX("%4", "%5", "%6", "%7", "%15", "%16") "}"
+                 : "+f"(acc[0][0]), "+f"(acc[0][1]), "+f"(acc[0][2]), "+f"(acc[0][3]),
+                   "+f"(acc[1][0]), "+f"(acc[1][1]), "+f"(acc[1][2]), "+f"(acc[1][3])
+                 : "r"(w), "r"(sub_r), "r"(add_r8), "r"(s_r), "r"(s_r8), "r"(b[0].x), "r"(b[0].y),
+                   "r"(b[1].x), "r"(b[1].y));
+  } else if constexpr (NB == 3) {
+    asm volatile("{\n\t" W4A16_DEQ_PTX("%12", "%13", "%14", "%15", "%16")
+                 W4A16_MMA_PTX("%0", "%1", "%2", "%3", "%17", "%18")
+                 W4A16_MMA_PTX("%4", "%5", "%6", "%7", "%19", "%20")
+                 W4A16_MMA_PTX("%8", "%9", "%10", "%11", "%21", "%22") "}"
+                 : "+f"(acc[0][0]), "+f"(acc[0][1]), "+f"(acc[0][2]), "+f"(acc[0][3]),
+                   "+f"(acc[1][0]), "+f"(acc[1][1]), "+f"(acc[1][2]), "+f"(acc[1][3]),
+                   "+f"(acc[2][0]), "+f"(acc[2][1]), "+f"(acc[2][2]), "+f"(acc[2][3])
+                 : "r"(w), "r"(sub_r), "r"(add_r8), "r"(s_r), "r"(s_r8), "r"(b[0].x), "r"(b[0].y),
+                   "r"(b[1].x), "r"(b[1].y), "r"(b[2].x), "r"(b[2].y));
+  } else {
+    static_assert(NB == 4, "NB must be 1..4");
+    asm volatile("{\n\t" W4A16_DEQ_PTX("%16", "%17", "%18", "%19", "%20")
+                 W4A16_MMA_PTX("%0", "%1", "%2", "%3", "%21", "%22")
+                 W4A16_MMA_PTX("%4", "%5", "%6", "%7", "%23", "%24")
+                 W4A16_MMA_PTX("%8", "%9", "%10", "%11", "%25", "%26")
+                 W4A16_MMA_PTX("%12", "%13", "%14", "%15", "%27", "%28") "}"
+                 : "+f"(acc[0][0]), "+f"(acc[0][1]), "+f"(acc[0][2]), "+f"(acc[0][3]),
+                   "+f"(acc[1][0]), "+f"(acc[1][1]), "+f"(acc[1][2]), "+f"(acc[1][3]),
+                   "+f"(acc[2][0]), "+f"(acc[2][1]), "+f"(acc[2][2]), "+f"(acc[2][3]),
+                   "+f"(acc[3][0]), "+f"(acc[3][1]), "+f"(acc[3][2]), "+f"(acc[3][3])
+                 : "r"(w), "r"(sub_r), "r"(add_r8), "r"(s_r), "r"(s_r8), "r"(b[0].x), "r"(b[0].y),
+                   "r"(b[1].x), "r"(b[1].y), "r"(b[2].x), "r"(b[2].y), "r"(b[3].x), "r"(b[3].y));
+  }
+}
+
 // Per-column constants of the dequantisation: 1024 + z and -(64 + z) as fp16
 // pairs, and the scale broadcast to both halves.
 struct ColConst {

@@ -63,9 +63,21 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 // NB: blocks of 8 tokens (M <= 8*NB).  JPW: 64-row chunks per consumer warp
 // per unit (a unit has 2*JPW chunks; warp half h takes chunks h*JPW .. +JPW-1).
-template <int NB, int JPW>
+// ZP: explicit zero points (else the implicit zero 8 is a constant).
+template <int NB, int JPW, bool ZP>
 __global__ void __launch_bounds__(kSmThreads, 1)
     w4a16_small_m_kernel(const __grid_constant__ CUtensorMap x_map, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -74,7 +86,6 @@ __global__ void __launch_bounds__(kSmThreads, 1)
   uint8_t* base = smem_raw + (base_addr - raw_addr);
   SmCtrl* ctrl = reinterpret_cast<SmCtrl*>(base);
   const uint32_t stage0 = base_addr + kCtrlBytes;
-  const uint8_t* stage0_ptr = base + kCtrlBytes;
   float* xchg = reinterpret_cast<float*>(base + kCtrlBytes + p.off_xchg);
 
   const int warp = threadIdx.x >> 5;
@@ -179,16 +190,27 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     const int r = lane >> 2;   // fragment row / token column within a block of 8
     const int c = lane & 3;
     const int col_r = 16 * g + r;  // this lane's two tile columns: col_r, col_r + 8
-    const bool has_zeros = p.zeros != nullptr;
     // X operand of k-step ks for token block nb: B column r reads token
     // xr = sigma(r) = 2(r%4) + r/4 of the block (so the four rows a half-warp
     // reads fall in four different 32-byte bank groups of the 128-byte
     // swizzle), rows k = 16ks + 4c .. +3 = 16-byte unit 2ks + c/2, swizzled by xr.
     const int xr = ((r & 3) << 1) | (r >> 2);
-    const uint32_t x_lane = (uint32_t)xr * 128 + (uint32_t)(c & 1) * 8;
-    uint32_t xoff[4];
+    uint32_t xoff[JPW][4];  // stage-relative byte offsets, per chunk and k-step
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks) xoff[ks] = (uint32_t)(((2 * ks + (c >> 1)) ^ xr) << 4);
+    for (int jj = 0; jj < JPW; ++jj)
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        xoff[jj][ks] = (uint32_t)(h * JPW + jj) * p.x_chunk_bytes + (uint32_t)xr * 128 +
+                       (uint32_t)(c & 1) * 8 + (uint32_t)(((2 * ks + (c >> 1)) ^ xr) << 4);
+    // stage-relative offsets of this lane's codes, scales and zeros; the
+    // warp's chunks lie in one group row: row h of the unit when a unit spans
+    // two groups (group 128, 256-row units), else row 0
+    const int gsub = (p.n_g > 1) ? h : 0;
+    const uint32_t code_off = p.off_codes + (uint32_t)(h * JPW) * kChunkCodeBytes +
+                              (uint32_t)(g * 32 + lane) * 16;
+    const uint32_t sc_off = p.off_scales + (uint32_t)(gsub * kTileN + col_r) * 2;
+    const uint32_t zr_off = p.off_zeros + (uint32_t)(gsub * (kTileN / 2) + (col_r >> 1));
+    const uint32_t z_shift = (uint32_t)(col_r & 1) * 4;
     // accumulator column 2c + e of a block is token sigma(2c + e)
     const int tok0 = (((2 * c) & 3) << 1) | ((2 * c) >> 2);
     const int tok1 = (((2 * c + 1) & 3) << 1) | ((2 * c + 1) >> 2);
@@ -208,36 +230,28 @@ __global__ void __launch_bounds__(kSmThreads, 1)
       for (int i = 0; i < seg_len; ++i) {
         if (!wait_warp(bar(ctrl->full[s]), ph, wc)) { ok = false; break; }
         const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
-        const uint8_t* st_ptr = stage0_ptr + (size_t)s * p.stage_bytes;
         uint4 wv[JPW];
 #pragma unroll
-        for (int jj = 0; jj < JPW; ++jj)
-          wv[jj] = lds128(st + p.off_codes + (uint32_t)(h * JPW + jj) * kChunkCodeBytes +
-                          (uint32_t)(g * 32 + lane) * 16);
-        // this warp's chunks lie in one group row: row h of the unit when a unit
-        // spans two groups (group 128, 256-row units), else row 0
-        const int gsub = (p.n_g > 1) ? h : 0;
-        const uint16_t* sc = reinterpret_cast<const uint16_t*>(st_ptr + p.off_scales) + gsub * kTileN;
-        uint32_t z0 = 8, z1 = 8;
-        if (has_zeros) {
-          const uint8_t* zb = st_ptr + p.off_zeros + gsub * (kTileN / 2);
-          z0 = (zb[col_r >> 1] >> ((col_r & 1) * 4)) & 0xFu;
-          z1 = (zb[(col_r + 8) >> 1] >> ((col_r & 1) * 4)) & 0xFu;
+        for (int jj = 0; jj < JPW; ++jj) wv[jj] = lds128(st + code_off + (uint32_t)jj * kChunkCodeBytes);
+        // implicit zero 8: 1024 + 8 and -(64 + 8) as fp16 pairs
+        uint32_t sub0 = 0x64086408u, add1 = 0xD480D480u;
+        if constexpr (ZP) {
+          const uint32_t zb0 = lds_u8(st + zr_off), zb1 = lds_u8(st + zr_off + 4);
+          const ColConst k0 = col_const(0, (zb0 >> z_shift) & 0xFu);
+          const ColConst k1 = col_const(0, (zb1 >> z_shift) & 0xFu);
+          sub0 = k0.sub; add1 = k1.add;
         }
-        const ColConst k0 = col_const(sc[col_r], z0), k1 = col_const(sc[col_r + 8], z1);
+        const uint32_t sr = lds_u16(st + sc_off), sr8 = lds_u16(st + sc_off + 16);
+        const uint32_t s0 = sr | (sr << 16), s1 = sr8 | (sr8 << 16);
 #pragma unroll
         for (int jj = 0; jj < JPW; ++jj) {
-          const uint32_t xs = st + (uint32_t)(h * JPW + jj) * p.x_chunk_bytes + x_lane;
           const uint32_t wk[4] = {wv[jj].x, wv[jj].y, wv[jj].z, wv[jj].w};
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            uint32_t a[4];
-            dequant_frag(wk[ks], k0.sub, k1.add, k0.s, k1.s, a);
+            uint2 b[NB];
 #pragma unroll
-            for (int nb = 0; nb < NB; ++nb) {
-              const uint2 b = lds64(xs + xoff[ks] + (uint32_t)nb * 1024);
-              mma_16816(acc[nb], a, b.x, b.y);
-            }
+            for (int nb = 0; nb < NB; ++nb) b[nb] = lds64(st + xoff[jj][ks] + (uint32_t)nb * 1024);
+            dequant_mma<NB>(acc, wk[ks], sub0, add1, s0, s1, b);
           }
         }
         __syncwarp();
@@ -359,13 +373,17 @@ __global__ void __launch_bounds__(kSmThreads, 1)
 
 }  // namespace
 
-#define W4A16_SMALL_M_KERNELS(X) X(1, 1) X(2, 1) X(3, 1) X(4, 1) X(1, 2) X(2, 2) X(3, 2) X(4, 2)
+#define W4A16_SMALL_M_KERNELS(X)                                                            \
+  X(1, 1, false) X(2, 1, false) X(3, 1, false) X(4, 1, false)                                \
+  X(1, 2, false) X(2, 2, false) X(3, 2, false) X(4, 2, false)                                \
+  X(1, 1, true) X(2, 1, true) X(3, 1, true) X(4, 1, true)                                    \
+  X(1, 2, true) X(2, 2, true) X(3, 2, true) X(4, 2, true)
 
 cudaError_t small_m_set_smem_limit(int bytes) {
   cudaError_t e = cudaSuccess;
-#define W4A16_SET(NB, JPW)                                                                   \
+#define W4A16_SET(NB, JPW, ZP)                                                               \
   if (e == cudaSuccess)                                                                      \
-    e = cudaFuncSetAttribute(w4a16_small_m_kernel<NB, JPW>,                                  \
+    e = cudaFuncSetAttribute(w4a16_small_m_kernel<NB, JPW, ZP>,                              \
                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   W4A16_SMALL_M_KERNELS(W4A16_SET)
 #undef W4A16_SET
@@ -385,8 +403,10 @@ cudaError_t launch_small_m(const CUtensorMap& x_map, const GemmParams& p, int gr
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-#define W4A16_LAUNCH(NB, JPW) \
-  if (nb == NB && jpw == JPW) return cudaLaunchKernelEx(&cfg, w4a16_small_m_kernel<NB, JPW>, x_map, p);
+  const bool zp = p.zeros != nullptr;
+#define W4A16_LAUNCH(NB, JPW, ZP)                                                          \
+  if (nb == NB && jpw == JPW && zp == ZP)                                                  \
+    return cudaLaunchKernelEx(&cfg, w4a16_small_m_kernel<NB, JPW, ZP>, x_map, p);
   W4A16_SMALL_M_KERNELS(W4A16_LAUNCH)
 #undef W4A16_LAUNCH
   return cudaErrorInvalidValue;
