@@ -97,7 +97,11 @@ GemmPlan make_plan(int M, int K, int N, int group, int sms, int smem_optin, bool
     g.kind = kKernelTcgen05;
     g.bn = M <= kMaxBn ? (int)round_up((size_t)M, 16) : kMaxBn;
     g.m_tiles = (M + g.bn - 1) / g.bn;
-    g.cpu = g.bn <= 64 ? 2 : 1;
+    // two MMA issuers (accumulators of bn columns each, one per dequant
+    // warpgroup and 64-row chunk of a 128-row unit) when both fit beside the A
+    // stages in tensor memory
+    g.nacc = g.bn <= 128 ? 2 : 1;
+    g.cpu = g.nacc == 2 ? 2 : 1;
   }
   g.kt = K / (kChunkK * g.cpu);
   g.n_g = (g.cpu * kChunkK > group) ? (g.cpu * kChunkK) / group : 1;
@@ -263,6 +267,9 @@ marlin_status_t marlin_gemm(const uint16_t* X, const void* packed, const uint16_
   p.tx_bytes = (uint32_t)g.cpu * (p.x_chunk_bytes + kChunkCodeBytes) + kTileN * 2 +
                (zeros ? kTileN / 2 : 0);
   p.weights_reused = g.m_tiles > 1;
+  p.nacc = g.nacc > 0 ? g.nacc : 1;
+  p.tx_w = (uint32_t)g.cpu * kChunkCodeBytes + (uint32_t)g.n_g * (kTileN * 2 + (zeros ? kTileN / 2 : 0));
+  p.tx_x = (uint32_t)g.cpu * p.x_chunk_bytes;
   p.n_g = g.n_g;
   p.units_per_group = g.upg;
   p.off_xchg = g.off_xchg;

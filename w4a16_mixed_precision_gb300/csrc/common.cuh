@@ -234,6 +234,55 @@ __device__ __forceinline__ void dequant_mma(float (&acc)[NB][4], uint32_t w, uin
   }
 }
 
+// Dequantise the four fragment words of one 16-column group (k-steps 0..3 of a
+// 64-row chunk) and store them to tensor memory as the A operand with one
+// tcgen05.st.16x256b.x4, all in one block of PTX (so the 16 results are
+// produced directly in the store's source registers).  Register order per
+// repetition: (col r, k..k+1), (col r, k+2..k+3), (col r+8, k..k+1),
+// (col r+8, k+2..k+3).
+#define W4A16_DEQW_PTX(W, SUB, ADD, S, S8, X)                          \
+  "shr.u32 w8, " W ", 8;\n\t"                                          \
+  "lop3.b32 t0_" X ", " W ", 0x000F000F, 0x64006400, 0xEA;\n\t"        \
+  "lop3.b32 t1_" X ", " W ", 0x00F000F0, 0x64006400, 0xEA;\n\t"        \
+  "lop3.b32 t2_" X ", w8, 0x000F000F, 0x64006400, 0xEA;\n\t"           \
+  "lop3.b32 t3_" X ", w8, 0x00F000F0, 0x64006400, 0xEA;\n\t"           \
+  "sub.rn.f16x2 t0_" X ", t0_" X ", " SUB ";\n\t"                      \
+  "fma.rn.f16x2 t1_" X ", t1_" X ", k16, " ADD ";\n\t"                 \
+  "sub.rn.f16x2 t2_" X ", t2_" X ", " SUB ";\n\t"                      \
+  "fma.rn.f16x2 t3_" X ", t3_" X ", k16, " ADD ";\n\t"                 \
+  "mul.rn.f16x2 t0_" X ", t0_" X ", " S ";\n\t"                        \
+  "mul.rn.f16x2 t1_" X ", t1_" X ", " S8 ";\n\t"                       \
+  "mul.rn.f16x2 t2_" X ", t2_" X ", " S ";\n\t"                        \
+  "mul.rn.f16x2 t3_" X ", t3_" X ", " S8 ";\n\t"
+
+__device__ __forceinline__ void dequant_store_tmem(uint32_t taddr, uint4 w, uint32_t sub_r,
+                                                   uint32_t add_r8, uint32_t s_r, uint32_t s_r8) {
+  asm volatile(
+      "{\n\t.reg .b32 w8, k16, t0_0, t1_0, t2_0, t3_0, t0_1, t1_1, t2_1, t3_1, t0_2, t1_2, t2_2, "
+      "t3_2, t0_3, t1_3, t2_3, t3_3;\n\t"
+      "mov.b32 k16, 0x2C002C00;\n\t"
+      W4A16_DEQW_PTX("%1", "%5", "%6", "%7", "%8", "0")
+      W4A16_DEQW_PTX("%2", "%5", "%6", "%7", "%8", "1")
+      W4A16_DEQW_PTX("%3", "%5", "%6", "%7", "%8", "2")
+      W4A16_DEQW_PTX("%4", "%5", "%6", "%7", "%8", "3")
+      "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {t0_0, t2_0, t1_0, t3_0, t0_1, t2_1, t1_1, "
+      "t3_1, t0_2, t2_2, t1_2, t3_2, t0_3, t2_3, t1_3, t3_3};\n\t"
+      "}" ::"r"(taddr),
+      "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w), "r"(sub_r), "r"(add_r8), "r"(s_r), "r"(s_r8)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 // Per-column constants of the dequantisation: 1024 + z and -(64 + z) as fp16
 // pairs, and the scale broadcast to both halves.
 struct ColConst {

@@ -40,7 +40,7 @@ struct Ctrl {
   uint64_t aempty[kAStages];
   uint64_t dfull;
   uint64_t dempty;
-  uint64_t drain;
+  uint64_t drain[2];
   uint64_t red_arrive;  // dequant warps -> leader: partial tile stored (contributor)
   uint64_t red_go;      // leader -> dequant warps: all partials published (reducer)
   uint32_t tmem_base;
@@ -66,7 +66,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* base = smem_raw + (base_addr - raw_addr);
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(base);
   const uint32_t stage0 = base_addr + kCtrlBytes;
-  const uint8_t* stage0_ptr = base + kCtrlBytes;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -84,24 +83,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtx wc{&ctrl->abort, p.status, p.timeout_ns};
 
   // ---- setup --------------------------------------------------------------------
+  const int nacc = p.nacc;
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(bar(ctrl->full[s]), 1);
-      mbar_init(bar(ctrl->empty[s]), 4 * cpu + 1);
+      mbar_init(bar(ctrl->full[s]), 2);                 // weights + activation producers
+      mbar_init(bar(ctrl->empty[s]), 4 * cpu + nacc);   // dequant warps + MMA issuers
     }
     for (int a = 0; a < kAStages; ++a) {
       mbar_init(bar(ctrl->afull[a]), 4);
       mbar_init(bar(ctrl->aempty[a]), 1);
     }
-    mbar_init(bar(ctrl->dfull), 1);
+    mbar_init(bar(ctrl->dfull), nacc);
     mbar_init(bar(ctrl->dempty), kNumDqWarps);
-    mbar_init(bar(ctrl->drain), 1);
+    mbar_init(bar(ctrl->drain[0]), 1);
+    mbar_init(bar(ctrl->drain[1]), 1);
     mbar_init(bar(ctrl->red_arrive), kNumDqWarps);
     mbar_init(bar(ctrl->red_go), 1);
     ctrl->abort = 0;
     fence_mbarrier_init();
-    prefetch_tensormap(&x_map);
   }
+  if (warp == 3 && lane == 0) prefetch_tensormap(&x_map);
   if (warp == 2) {
     tmem_alloc(smem_addr(&ctrl->tmem_base), kTmemCols);
     tmem_relinquish();
@@ -118,10 +119,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   griddep_wait();
 
   if (warp == 0) {
-    // ================= producer: TMA into the stage ring =================
+    // ================= weights producer: codes, scales, zeros =================
     if (lane == 0) {
       const uint64_t pol_w = p.weights_reused ? policy_evict_last() : policy_evict_first();
-      const uint64_t pol_x = policy_evict_last();
       const uint8_t* codes = reinterpret_cast<const uint8_t*>(p.codes);
       const int KB = p.K / kChunkK;
       const uint32_t code_bytes = (uint32_t)(cpu * kChunkCodeBytes);
@@ -130,23 +130,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       int nt = tile_begin - mt * p.n_tiles;
       int ku = ku_begin;
       int g = ku / units_per_group, ku_in_g = ku - g * units_per_group;
-      int s = 0;
+      int s = 0, issued = 0;
       uint32_t ph = 0;
-      int issued = 0;
       for (int u = u_begin; u < u_end; ++u) {
         if (!wait_thread(bar(ctrl->empty[s]), ph ^ 1u, wc)) break;
-        const int k0 = ku * cpu * kChunkK;
         const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
         const uint32_t fb = bar(ctrl->full[s]);
-        mbar_arrive_expect_tx(fb, p.tx_bytes);
+        mbar_arrive_expect_tx(fb, p.tx_w);
         bulk_g2s(st + p.off_codes, codes + ((size_t)nt * KB + (size_t)ku * cpu) * kChunkCodeBytes,
                  code_bytes, fb, pol_w);
         const size_t grow = (size_t)nt * p.G + g;  // tile-major group row
         bulk_g2s(st + p.off_scales, p.scales + grow * kTileN, kTileN * 2, fb, pol_w);
         if (p.zeros) bulk_g2s(st + p.off_zeros, p.zeros + grow * (kTileN / 2), kTileN / 2, fb, pol_w);
-        for (int j = 0; j < cpu; ++j)
-          tma_load_2d(st + (uint32_t)j * p.x_chunk_bytes, &x_map, k0 + j * kChunkK, mt * p.bn, fb,
-                      pol_x);
         ++issued;
         if (++s == S) { s = 0; ph ^= 1u; }
         if (++ku_in_g == units_per_group) { ku_in_g = 0; ++g; }
@@ -160,10 +155,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = first; i < issued; ++i)
         wait_drain(bar(ctrl->full[i % S]), (uint32_t)((i / S) & 1), wc);
     }
-  } else if (warp == 1) {
-    // ================= MMA issuer (one thread) =================
+  } else if (warp == 3) {
+    // ================= activation producer: X tiles =================
     if (lane == 0) {
+      const uint64_t pol_x = policy_evict_last();
+      int mt = tile_begin / p.n_tiles;
+      int nt = tile_begin - mt * p.n_tiles;
+      int ku = ku_begin;
+      int s = 0, issued = 0;
+      uint32_t ph = 0;
+      for (int u = u_begin; u < u_end; ++u) {
+        if (!wait_thread(bar(ctrl->empty[s]), ph ^ 1u, wc)) break;
+        const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
+        const uint32_t fb = bar(ctrl->full[s]);
+        mbar_arrive_expect_tx(fb, p.tx_x);
+        const int k0 = ku * cpu * kChunkK;
+        for (int j = 0; j < cpu; ++j)
+          tma_load_2d(st + (uint32_t)j * p.x_chunk_bytes, &x_map, k0 + j * kChunkK, mt * p.bn, fb,
+                      pol_x);
+        ++issued;
+        if (++s == S) { s = 0; ph ^= 1u; }
+        if (++ku == KT) {
+          ku = 0;
+          if (++nt == p.n_tiles) { nt = 0; ++mt; }
+        }
+      }
+      const int first = issued > S ? issued - S : 0;
+      for (int i = first; i < issued; ++i)
+        wait_drain(bar(ctrl->full[i % S]), (uint32_t)((i / S) & 1), wc);
+    }
+  } else if (warp == 1 || warp == 2) {
+    // ================= MMA issuers (one thread each) =================
+    // Issuer i takes chunk j == i of every 128-row unit into its own
+    // accumulator (two issuers), or every chunk (one issuer).
+    const int iss = warp - 1;
+    if (lane == 0 && iss < nacc) {
       const uint32_t idesc = umma_idesc_f16_f32((uint32_t)p.bn);
+      const uint32_t d_tmem = tmem + (uint32_t)(iss * p.bn);
       int s = 0, a = 0, seg = 0;
       uint32_t ph = 0, aph = 0;
       int u = u_begin, ku = ku_begin;
@@ -179,17 +207,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_thread(bar(ctrl->full[s]), ph, wc)) { ok = false; break; }
           const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
           for (int j = 0; j < cpu; ++j) {
-            if (!wait_thread(bar(ctrl->afull[a]), aph, wc)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t xs = st + (uint32_t)j * p.x_chunk_bytes;
-            const uint32_t a_col = tmem + kAColBase + (uint32_t)a * (kChunkK / 2);
+            if (nacc == 1 || j == iss) {
+              if (!wait_thread(bar(ctrl->afull[a]), aph, wc)) { ok = false; break; }
+              tc_fence_after();
+              const uint32_t xs = st + (uint32_t)j * p.x_chunk_bytes;
+              const uint32_t a_col = tmem + kAColBase + (uint32_t)a * (kChunkK / 2);
+              const uint64_t desc0 = umma_desc_sw128(xs);
 #pragma unroll
-            for (int kk = 0; kk < kChunkK / 16; ++kk) {
-              mma_f16_ts(tmem, a_col + (uint32_t)kk * 8, umma_desc_sw128(xs + (uint32_t)kk * 32),
-                         idesc, acc);
-              acc = 1;
+              for (int kk = 0; kk < kChunkK / 16; ++kk) {
+                // +32 bytes per 16-row step = +2 in the descriptor's address field
+                mma_f16_ts(d_tmem, a_col + (uint32_t)kk * 8, desc0 + (uint64_t)(2 * kk), idesc, acc);
+                acc = 1;
+              }
+              mma_commit(bar(ctrl->aempty[a]));
             }
-            mma_commit(bar(ctrl->aempty[a]));
             if (++a == kAStages) { a = 0; aph ^= 1u; }
           }
           if (!ok) break;
@@ -203,8 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ku = 0;
       }
       // Every issued MMA must finish before TMEM is released.
-      mma_commit(bar(ctrl->drain));
-      wait_drain(bar(ctrl->drain), 0, wc);
+      mma_commit(bar(ctrl->drain[iss]));
+      wait_drain(bar(ctrl->drain[iss]), 0, wc);
     }
   } else if (warp >= kFirstDqWarp) {
     // ================= dequantisation + epilogue (8 warps) =================
@@ -215,8 +246,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const bool has_zeros = p.zeros != nullptr;
     // dequantisation: this thread holds fragment lane `lane` of the two 16-column
-    // groups 2*quarter and 2*quarter+1, i.e. columns fr + {0, 8} of each
-    const int fr = lane >> 2;
+    // groups 2*quarter and 2*quarter+1, i.e. columns c0 + {0, 8, 16, 24}
+    const int c0 = 32 * quarter + (lane >> 2);
+    const uint32_t code_off = p.off_codes + (uint32_t)((2 * quarter) * 32 + lane) * 16;
+    const uint32_t sc_off = p.off_scales + (uint32_t)c0 * 2;
+    const uint32_t zr_off = p.off_zeros + (uint32_t)(c0 >> 1);
+    const uint32_t z_shift = (uint32_t)(c0 & 1) * 4;
     int s = 0, a = 0, ch = 0, seg = 0;
     uint32_t ph = 0, aph = 0;
     int u = u_begin, ku = ku_begin, tile = tile_begin;
@@ -228,54 +263,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- mainloop: dequantise this warpgroup's chunks into TMEM ----
       for (int i = 0; i < seg_len && ok; ++i) {
         const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
-        const uint8_t* st_ptr = stage0_ptr + (size_t)s * p.stage_bytes;
         for (int j = 0; j < cpu; ++j) {
           if ((ch & 1) == wg) {
             if (!wait_warp(bar(ctrl->full[s]), ph, wc)) { ok = false; break; }
-            const uint32_t cw = st + p.off_codes + (uint32_t)j * kChunkCodeBytes +
-                                (uint32_t)((2 * quarter) * 32 + lane) * 16;
+            const uint32_t cw = st + code_off + (uint32_t)j * kChunkCodeBytes;
             const uint4 w0 = lds128(cw);        // group 2q, k-steps 0..3
             const uint4 w1 = lds128(cw + 512);  // group 2q+1
-            const uint16_t* sc = reinterpret_cast<const uint16_t*>(st_ptr + p.off_scales);
-            const int c0 = 32 * quarter + fr;   // columns c0, c0+8, c0+16, c0+24
             uint32_t z0 = 8, z1 = 8, z2 = 8, z3 = 8;
             if (has_zeros) {
-              const uint8_t* zb = st_ptr + p.off_zeros;
-              z0 = (zb[(c0) >> 1] >> ((c0 & 1) * 4)) & 0xFu;
-              z1 = (zb[(c0 + 8) >> 1] >> ((c0 & 1) * 4)) & 0xFu;
-              z2 = (zb[(c0 + 16) >> 1] >> ((c0 & 1) * 4)) & 0xFu;
-              z3 = (zb[(c0 + 24) >> 1] >> ((c0 & 1) * 4)) & 0xFu;
+              z0 = (lds_u8(st + zr_off) >> z_shift) & 0xFu;
+              z1 = (lds_u8(st + zr_off + 4) >> z_shift) & 0xFu;
+              z2 = (lds_u8(st + zr_off + 8) >> z_shift) & 0xFu;
+              z3 = (lds_u8(st + zr_off + 12) >> z_shift) & 0xFu;
             }
-            const ColConst k0 = col_const(sc[c0], z0), k1 = col_const(sc[c0 + 8], z1);
-            const ColConst k2 = col_const(sc[c0 + 16], z2), k3 = col_const(sc[c0 + 24], z3);
+            const ColConst k0 = col_const((uint16_t)lds_u16(st + sc_off), z0);
+            const ColConst k1 = col_const((uint16_t)lds_u16(st + sc_off + 16), z1);
+            const ColConst k2 = col_const((uint16_t)lds_u16(st + sc_off + 32), z2);
+            const ColConst k3 = col_const((uint16_t)lds_u16(st + sc_off + 48), z3);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(ctrl->empty[s]));
 
-            // tcgen05.st.16x256b order per k-step: (col r, k..k+1), (col r, k+2..k+3),
-            // (col r+8, k..k+1), (col r+8, k+2..k+3)
-            uint32_t v0[16], v1[16];
-            const uint32_t wa[4] = {w0.x, w0.y, w0.z, w0.w};
-            const uint32_t wb[4] = {w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              uint32_t h[4];
-              dequant_frag(wa[ks], k0.sub, k1.add, k0.s, k1.s, h);
-              v0[4 * ks + 0] = h[0];
-              v0[4 * ks + 1] = h[2];
-              v0[4 * ks + 2] = h[1];
-              v0[4 * ks + 3] = h[3];
-              dequant_frag(wb[ks], k2.sub, k3.add, k2.s, k3.s, h);
-              v1[4 * ks + 0] = h[0];
-              v1[4 * ks + 1] = h[2];
-              v1[4 * ks + 2] = h[1];
-              v1[4 * ks + 3] = h[3];
-            }
-
             if (!wait_warp(bar(ctrl->aempty[a]), aph ^ 1u, wc)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t acol = tmem + kAColBase + (uint32_t)a * (kChunkK / 2);
-            tmem_st_16x256b_x4(acol + lane_off, v0);
-            tmem_st_16x256b_x4(acol + lane_off + (16u << 16), v1);
+            const uint32_t acol = tmem + kAColBase + (uint32_t)a * (kChunkK / 2) + lane_off;
+            dequant_store_tmem(acol, w0, k0.sub, k1.add, k0.s, k1.s);
+            dequant_store_tmem(acol + (16u << 16), w1, k2.sub, k3.add, k2.s, k3.s);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -313,12 +325,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float* part = p.partials + (size_t)blockIdx.x * ((size_t)p.bn * kTileN);
       for (int cc = wg; cc < p.bn / 8; cc += 2) {
-        uint32_t r[8];
+        uint32_t r[8], r1[8];
         tmem_ld_x8(tmem + lane_off + (uint32_t)cc * 8, r);
+        if (nacc == 2) tmem_ld_x8(tmem + lane_off + (uint32_t)(p.bn + cc * 8), r1);
         tmem_wait_ld();
         float acc[8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) acc[c] = __uint_as_float(r[c]);
+        for (int c = 0; c < 8; ++c)
+          acc[c] = nacc == 2 ? __uint_as_float(r[c]) + __uint_as_float(r1[c]) : __uint_as_float(r[c]);
         if (reducer) {
           // own partial first, then the others' in stripe order (fixed order,
           // bit-reproducible); loads of 4 contributors are issued together

@@ -9,7 +9,7 @@
 namespace w4a16 {
 
 // Fixed geometry of the fused kernel.
-constexpr int kThreads = 384;      // 12 warps: producer, MMA, TMEM owner, spare, 8 dequant
+constexpr int kThreads = 384;      // 12 warps: 2 producers, 2 MMA issuers (one owns TMEM), 8 dequant
 constexpr int kTileN = 128;        // output columns per tile = UMMA M
 constexpr int kChunkK = 64;        // K elements per dequantised A chunk
 constexpr int kChunkCodeBytes = kTileN * kChunkK / 2;  // 4096
@@ -43,6 +43,8 @@ struct GemmParams {
   uint32_t off_codes, off_scales, off_zeros;  // byte offsets inside a stage
   uint32_t tx_bytes;        // bytes landed per stage
   int weights_reused;       // more than one m-tile reads the same weights
+  int nacc;                 // tcgen05 kernel: MMA issuers, each with its own accumulator (1 or 2)
+  uint32_t tx_w, tx_x;      // bytes landed per stage by the weights / activation producer
   int n_g;                  // scale/zero group rows per unit (2 only for group 128, 256-row units)
   int units_per_group;      // units per group row (>= 1)
   uint32_t off_xchg;        // small-M kernel: exchange buffer, bytes after stage 0
@@ -53,7 +55,7 @@ struct GemmParams {
 enum KernelKind { kKernelTcgen05 = 0, kKernelSmallM = 1 };
 struct GemmPlan {
   int kind;
-  int bn, m_tiles, n_tiles, kt, cpu, stages, grid, n_g, upg;
+  int bn, m_tiles, n_tiles, kt, cpu, stages, grid, n_g, upg, nacc;
   uint32_t off_xchg;
   long long units;
   uint32_t stage_bytes, smem_bytes;
