@@ -115,6 +115,8 @@ GemmPlan make_plan(int M, int K, int N, int group, int sms, int smem_optin, bool
   const size_t xchg = g.kind == kKernelSmallM ? (size_t)4 * (g.bn / 8) * 256 * sizeof(float) : 0;
   int stages = (int)((budget - (long long)xchg) / (long long)g.stage_bytes);
   if (stages > kMaxStages) stages = kMaxStages;
+  // tcgen05 kernel: each consumer takes a fixed residue of the unit index mod 4
+  if (g.kind == kKernelTcgen05) stages &= ~3;
   g.stages = stages;
   g.off_xchg = (uint32_t)((size_t)stages * g.stage_bytes);
   g.smem_bytes = (uint32_t)(kCtrlBytes + 1024 + (size_t)stages * g.stage_bytes + xchg);

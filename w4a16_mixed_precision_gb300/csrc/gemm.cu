@@ -13,15 +13,16 @@
 //     ("Marlin Project Overview", section "Key Techniques").  Column tiles cut by
 //     a stripe boundary are summed through an fp32 workspace by the CTA owning
 //     the tile's first unit, in a fixed order, so results are bit-reproducible.
-//   * Warp roles: warp 0 streams packed codes, scales, zeros (bulk TMA) and X
-//     (tensor TMA, 128-byte swizzle) through a multi-stage mbarrier ring in shared
-//     memory ("Marlin", section "async copy and pipeline"); warps 4..11 (two
-//     warpgroups, alternating chunks) turn 4-bit codes into fp16 with the
-//     0x6400 exponent trick, scale them with one fp16 multiply, and store the
-//     result straight into tensor memory as the A operand; warp 1 issues
-//     tcgen05.mma (A from TMEM, B = X from shared memory, fp32 accumulators in
-//     TMEM); the dequant warps then read the accumulators back with tcgen05.ld
-//     and write fp16 Y (or fp32 partials).
+//   * Warp roles: warp 0 streams packed codes, scales, zeros (bulk TMA) and
+//     warp 3 streams X (tensor TMA, 128-byte swizzle) through a multi-stage
+//     mbarrier ring in shared memory ("Marlin", section "async copy and
+//     pipeline"); warps 4..19 (four warpgroups, taking whole units in turn)
+//     turn 4-bit codes into fp16 with the 0x6400 exponent trick, scale them
+//     with one fp16 multiply, and store the result straight into tensor memory
+//     as the A operand; warps 1 and 2 issue tcgen05.mma for alternate units of
+//     a tile (A from TMEM, B = X from shared memory, fp32 accumulators in
+//     TMEM, one each); the dequant warps then read the accumulators back with
+//     tcgen05.ld and write fp16 Y (or fp32 partials).
 //   * Every wait is bounded (global timer); on expiry the kernel records
 //     kStatusTimeout in the status word, drains its own copies and MMAs, frees
 //     TMEM and returns.
@@ -48,8 +49,12 @@ struct Ctrl {
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
 
-constexpr int kNumDqWarps = 8;
+constexpr int kNumDqWG = 4;                // dequant warpgroups
+constexpr int kNumDqWarps = 4 * kNumDqWG;
 constexpr int kFirstDqWarp = 4;
+static_assert((kNumDqWG & (kNumDqWG - 1)) == 0, "unit residues need a power-of-two warpgroup count");
+static_assert((kAStages / 2) % kNumDqWG == 0, "A slots must be a multiple of the warpgroup count");
+static_assert(kThreads == 32 * (kFirstDqWarp + kNumDqWarps), "block size");
 
 // ---- the kernel -----------------------------------------------------------------
 //
@@ -87,7 +92,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(bar(ctrl->full[s]), 2);                 // weights + activation producers
-      mbar_init(bar(ctrl->empty[s]), 4 * cpu + nacc);   // dequant warps + MMA issuers
+      mbar_init(bar(ctrl->empty[s]), 4 + 1);            // one dequant warpgroup + one MMA issuer
     }
     for (int a = 0; a < kAStages; ++a) {
       mbar_init(bar(ctrl->afull[a]), 4);
@@ -186,12 +191,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1 || warp == 2) {
     // ================= MMA issuers (one thread each) =================
-    // Issuer i takes chunk j == i of every 128-row unit into its own
-    // accumulator (two issuers), or every chunk (one issuer).
+    // With two issuers, issuer i takes the units i, i+2, ... of the stripe into
+    // its own accumulator; with one, every unit.  Every barrier ring is indexed
+    // by the stripe's unit index, and each consumer of a ring takes a fixed
+    // residue of it (issuer: unit mod 2, dequant warpgroup: unit mod 4; the
+    // stage count and the A slots are multiples of 4), so a consumer is never
+    // more than one phase ahead of a barrier it waits on.
     const int iss = warp - 1;
     if (lane == 0 && iss < nacc) {
       const uint32_t idesc = umma_idesc_f16_f32((uint32_t)p.bn);
       const uint32_t d_tmem = tmem + (uint32_t)(iss * p.bn);
+      const int a_slots = kAStages / cpu;
+      const uint32_t a_cols = (uint32_t)cpu * (kChunkK / 2);
       int s = 0, a = 0, seg = 0;
       uint32_t ph = 0, aph = 0;
       int u = u_begin, ku = ku_begin;
@@ -203,32 +214,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
         }
         uint32_t acc = 0;
-        for (int i = 0; i < seg_len && ok; ++i) {
-          if (!wait_thread(bar(ctrl->full[s]), ph, wc)) { ok = false; break; }
-          const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
-          for (int j = 0; j < cpu; ++j) {
-            if (nacc == 1 || j == iss) {
-              if (!wait_thread(bar(ctrl->afull[a]), aph, wc)) { ok = false; break; }
-              tc_fence_after();
-              const uint32_t xs = st + (uint32_t)j * p.x_chunk_bytes;
-              const uint32_t a_col = tmem + kAColBase + (uint32_t)a * (kChunkK / 2);
-              const uint64_t desc0 = umma_desc_sw128(xs);
+        for (int i = 0; i < seg_len; ++i) {
+          if (((u - u_begin + i) & (nacc - 1)) == iss) {
+            if (!wait_thread(bar(ctrl->full[s]), ph, wc)) { ok = false; break; }
+            if (!wait_thread(bar(ctrl->afull[a]), aph, wc)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
+            const uint32_t a_col = tmem + kAColBase + (uint32_t)a * a_cols;
+            for (int j = 0; j < cpu; ++j) {
+              const uint64_t desc0 = umma_desc_sw128(st + (uint32_t)j * p.x_chunk_bytes);
 #pragma unroll
               for (int kk = 0; kk < kChunkK / 16; ++kk) {
                 // +32 bytes per 16-row step = +2 in the descriptor's address field
-                mma_f16_ts(d_tmem, a_col + (uint32_t)kk * 8, desc0 + (uint64_t)(2 * kk), idesc, acc);
+                mma_f16_ts(d_tmem, a_col + (uint32_t)(j * (kChunkK / 2) + kk * 8),
+                           desc0 + (uint64_t)(2 * kk), idesc, acc);
                 acc = 1;
               }
-              mma_commit(bar(ctrl->aempty[a]));
             }
-            if (++a == kAStages) { a = 0; aph ^= 1u; }
+            mma_commit(bar(ctrl->aempty[a]));
+            mma_commit(bar(ctrl->empty[s]));
           }
-          if (!ok) break;
-          mma_commit(bar(ctrl->empty[s]));
+          if (++a == a_slots) { a = 0; aph ^= 1u; }
           if (++s == S) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
-        mma_commit(bar(ctrl->dfull));
+        // an issuer without a unit in this segment has nothing in flight for it
+        if (acc) mma_commit(bar(ctrl->dfull));
+        else mbar_arrive(bar(ctrl->dfull));
         ++seg;
         u += seg_len;
         ku = 0;
@@ -238,9 +250,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_drain(bar(ctrl->drain[iss]), 0, wc);
     }
   } else if (warp >= kFirstDqWarp) {
-    // ================= dequantisation + epilogue (8 warps) =================
-    const int dq = warp - kFirstDqWarp;       // 0..7
-    const int wg = dq >> 2;                   // warpgroup: even / odd chunks
+    // ================= dequantisation + epilogue (16 warps) =================
+    const int dq = warp - kFirstDqWarp;       // 0..11
+    const int wg = dq >> 2;                   // warpgroup: takes every fourth unit
     const int quarter = warp & 3;             // TMEM lane quarter this warp may touch
     const int row = quarter * 32 + lane;      // epilogue: output column within the tile
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
@@ -252,7 +264,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sc_off = p.off_scales + (uint32_t)c0 * 2;
     const uint32_t zr_off = p.off_zeros + (uint32_t)(c0 >> 1);
     const uint32_t z_shift = (uint32_t)(c0 & 1) * 4;
-    int s = 0, a = 0, ch = 0, seg = 0;
+    const int a_slots = kAStages / cpu;
+    const uint32_t a_cols = (uint32_t)cpu * (kChunkK / 2);
+    int s = 0, a = 0, seg = 0;
     uint32_t ph = 0, aph = 0;
     int u = u_begin, ku = ku_begin, tile = tile_begin;
     bool ok = true;
@@ -260,42 +274,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int seg_len = min(u_end - u, KT - ku);
       const int mt = tile / p.n_tiles;
       const int nt = tile - mt * p.n_tiles;
-      // ---- mainloop: dequantise this warpgroup's chunks into TMEM ----
-      for (int i = 0; i < seg_len && ok; ++i) {
-        const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
-        for (int j = 0; j < cpu; ++j) {
-          if ((ch & 1) == wg) {
-            if (!wait_warp(bar(ctrl->full[s]), ph, wc)) { ok = false; break; }
-            const uint32_t cw = st + code_off + (uint32_t)j * kChunkCodeBytes;
-            const uint4 w0 = lds128(cw);        // group 2q, k-steps 0..3
-            const uint4 w1 = lds128(cw + 512);  // group 2q+1
-            uint32_t z0 = 8, z1 = 8, z2 = 8, z3 = 8;
-            if (has_zeros) {
-              z0 = (lds_u8(st + zr_off) >> z_shift) & 0xFu;
-              z1 = (lds_u8(st + zr_off + 4) >> z_shift) & 0xFu;
-              z2 = (lds_u8(st + zr_off + 8) >> z_shift) & 0xFu;
-              z3 = (lds_u8(st + zr_off + 12) >> z_shift) & 0xFu;
+      // ---- mainloop: dequantise this warpgroup's units into TMEM ----
+      for (int i = 0; i < seg_len; ++i) {
+        if (((u - u_begin + i) & (kNumDqWG - 1)) == wg) {
+          if (!wait_warp(bar(ctrl->full[s]), ph, wc)) { ok = false; break; }
+          const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
+          // a unit (cpu <= 2 chunks of 64 rows, group >= 128) lies in one group row
+          uint4 w0[2], w1[2];
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            if (j < cpu) {
+              w0[j] = lds128(st + code_off + (uint32_t)j * kChunkCodeBytes);        // group 2q
+              w1[j] = lds128(st + code_off + (uint32_t)j * kChunkCodeBytes + 512);  // group 2q+1
             }
-            const ColConst k0 = col_const((uint16_t)lds_u16(st + sc_off), z0);
-            const ColConst k1 = col_const((uint16_t)lds_u16(st + sc_off + 16), z1);
-            const ColConst k2 = col_const((uint16_t)lds_u16(st + sc_off + 32), z2);
-            const ColConst k3 = col_const((uint16_t)lds_u16(st + sc_off + 48), z3);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(ctrl->empty[s]));
-
-            if (!wait_warp(bar(ctrl->aempty[a]), aph ^ 1u, wc)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t acol = tmem + kAColBase + (uint32_t)a * (kChunkK / 2) + lane_off;
-            dequant_store_tmem(acol, w0, k0.sub, k1.add, k0.s, k1.s);
-            dequant_store_tmem(acol + (16u << 16), w1, k2.sub, k3.add, k2.s, k3.s);
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(ctrl->afull[a]));
+          uint32_t z0 = 8, z1 = 8, z2 = 8, z3 = 8;
+          if (has_zeros) {
+            z0 = (lds_u8(st + zr_off) >> z_shift) & 0xFu;
+            z1 = (lds_u8(st + zr_off + 4) >> z_shift) & 0xFu;
+            z2 = (lds_u8(st + zr_off + 8) >> z_shift) & 0xFu;
+            z3 = (lds_u8(st + zr_off + 12) >> z_shift) & 0xFu;
           }
-          ++ch;
-          if (++a == kAStages) { a = 0; aph ^= 1u; }
+          const ColConst k0 = col_const((uint16_t)lds_u16(st + sc_off), z0);
+          const ColConst k1 = col_const((uint16_t)lds_u16(st + sc_off + 16), z1);
+          const ColConst k2 = col_const((uint16_t)lds_u16(st + sc_off + 32), z2);
+          const ColConst k3 = col_const((uint16_t)lds_u16(st + sc_off + 48), z3);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(ctrl->empty[s]));
+
+          if (!wait_warp(bar(ctrl->aempty[a]), aph ^ 1u, wc)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t acol = tmem + kAColBase + (uint32_t)a * a_cols + lane_off;
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            if (j < cpu) {
+              const uint32_t cj = acol + (uint32_t)j * (kChunkK / 2);
+              dequant_store_tmem(cj, w0[j], k0.sub, k1.add, k0.s, k1.s);
+              dequant_store_tmem(cj + (16u << 16), w1[j], k2.sub, k3.add, k2.s, k3.s);
+            }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(ctrl->afull[a]));
         }
+        if (++a == a_slots) { a = 0; aph ^= 1u; }
         if (++s == S) { s = 0; ph ^= 1u; }
       }
       if (!ok) break;
@@ -324,22 +345,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (*reinterpret_cast<volatile int*>(&ctrl->abort)) break;
       }
       float* part = p.partials + (size_t)blockIdx.x * ((size_t)p.bn * kTileN);
-      for (int cc = wg; cc < p.bn / 8; cc += 2) {
+      // accumulators holding units of this tile: both, or the one of its only unit
+      const bool two = nacc == 2 && seg_len >= 2;
+      const uint32_t d_first = (nacc == 2 && seg_len == 1) ? (uint32_t)(((u - u_begin) & 1) * p.bn) : 0u;
+      for (int cc = wg; cc < p.bn / 8; cc += kNumDqWG) {
         uint32_t r[8], r1[8];
-        tmem_ld_x8(tmem + lane_off + (uint32_t)cc * 8, r);
-        if (nacc == 2) tmem_ld_x8(tmem + lane_off + (uint32_t)(p.bn + cc * 8), r1);
+        tmem_ld_x8(tmem + lane_off + d_first + (uint32_t)cc * 8, r);
+        if (two) tmem_ld_x8(tmem + lane_off + (uint32_t)(p.bn + cc * 8), r1);
         tmem_wait_ld();
         float acc[8];
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-          acc[c] = nacc == 2 ? __uint_as_float(r[c]) + __uint_as_float(r1[c]) : __uint_as_float(r[c]);
+          acc[c] = two ? __uint_as_float(r[c]) + __uint_as_float(r1[c]) : __uint_as_float(r[c]);
         if (reducer) {
           // own partial first, then the others' in stripe order (fixed order,
-          // bit-reproducible); loads of 4 contributors are issued together
-          for (long long q0 = c_first + 1; q0 <= c_last; q0 += 4) {
-            float v[4][8];
+          // bit-reproducible); loads of 2 contributors are issued together
+          for (long long q0 = c_first + 1; q0 <= c_last; q0 += 2) {
+            float v[2][8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 2; ++j) {
               if (q0 + j <= c_last) {
                 const float* qp = p.partials + (size_t)(q0 + j) * ((size_t)p.bn * kTileN) +
                                   (size_t)(cc * 8) * kTileN + row;
@@ -348,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < 2; ++j)
               if (q0 + j <= c_last) {
 #pragma unroll
                 for (int c = 0; c < 8; ++c) acc[c] += v[j][c];
@@ -372,16 +396,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       if (!whole && !reducer) {
         // contributor (this is its first segment): publish the partial tile
-        // with one release increment and go on.  The warps' stores are ordered
-        // before it by the CTA-scoped mbarrier and the leader's gpu fence.
+        // with one release increment and go on.
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(ctrl->red_arrive));
         if (dq == 0) {
           if (!wait_warp(bar(ctrl->red_arrive), 0, wc)) break;
-          if (lane == 0) {
-            __threadfence();
-            red_release_gpu_add(&p.counters[tile], 1);
-          }
+          // the release is cumulative: it also orders the other warps'
+          // stores, which this thread observed through the mbarrier
+          if (lane == 0) red_release_gpu_add(&p.counters[tile], 1);
           __syncwarp();
         }
       }

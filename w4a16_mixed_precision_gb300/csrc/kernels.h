@@ -9,7 +9,7 @@
 namespace w4a16 {
 
 // Fixed geometry of the fused kernel.
-constexpr int kThreads = 384;      // 12 warps: 2 producers, 2 MMA issuers (one owns TMEM), 8 dequant
+constexpr int kThreads = 640;      // 20 warps: 2 producers, 2 MMA issuers (one owns TMEM), 16 dequant
 constexpr int kTileN = 128;        // output columns per tile = UMMA M
 constexpr int kChunkK = 64;        // K elements per dequantised A chunk
 constexpr int kChunkCodeBytes = kTileN * kChunkK / 2;  // 4096

@@ -289,10 +289,9 @@ __global__ void __launch_bounds__(kSmThreads, 1)
             if (lane == 0) mbar_arrive(bar(ctrl->red_arrive));
             if (g == 0) {
               if (!wait_warp(bar(ctrl->red_arrive), 0, wc)) break;
-              if (lane == 0) {
-                __threadfence();
-                red_release_gpu_add(&p.counters[tile], 1);
-              }
+              // the release is cumulative: it also orders the other warps'
+              // stores, which this thread observed through the mbarrier
+              if (lane == 0) red_release_gpu_add(&p.counters[tile], 1);
               __syncwarp();
             }
           } else {
@@ -311,10 +310,10 @@ __global__ void __launch_bounds__(kSmThreads, 1)
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) {
               float tot[4] = {acc[nb][0], acc[nb][1], acc[nb][2], acc[nb][3]};
-              for (long long q0 = c_first + 1; q0 <= c_last; q0 += 4) {
-                float v[4][4];
+              for (long long q0 = c_first + 1; q0 <= c_last; q0 += 8) {
+                float v[8][4];
 #pragma unroll
-                for (int jq = 0; jq < 4; ++jq) {
+                for (int jq = 0; jq < 8; ++jq) {
                   if (q0 + jq <= c_last) {
                     const float* qp = p.partials + (size_t)(q0 + jq) * ((size_t)p.bn * kTileN);
 #pragma unroll
@@ -324,7 +323,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
                   }
                 }
 #pragma unroll
-                for (int jq = 0; jq < 4; ++jq)
+                for (int jq = 0; jq < 8; ++jq)
                   if (q0 + jq <= c_last) {
 #pragma unroll
                     for (int d = 0; d < 4; ++d) tot[d] += v[jq][d];
