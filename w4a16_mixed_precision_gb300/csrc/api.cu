@@ -102,6 +102,13 @@ GemmPlan make_plan(int M, int K, int N, int group, int sms, int smem_optin, bool
     // stages in tensor memory
     g.nacc = g.bn <= 128 ? 2 : 1;
     g.cpu = g.nacc == 2 ? 2 : 1;
+    // A slots (one unit of cpu*64 rows = cpu*32 columns each) fill the tensor
+    // memory above the accumulators; an even count of at least 4 keeps every
+    // waiter within one phase of the slot barriers
+    const int a_cols = g.cpu * kChunkK / 2;
+    int slots = (kTmemCols - g.nacc * g.bn) / a_cols;
+    if (slots > kAStages) slots = kAStages;
+    g.a_slots = slots & ~1;
   }
   g.kt = K / (kChunkK * g.cpu);
   g.n_g = (g.cpu * kChunkK > group) ? (g.cpu * kChunkK) / group : 1;
@@ -218,6 +225,7 @@ marlin_status_t marlin_gemm(const uint16_t* X, const void* packed, const uint16_
 
   const GemmPlan g = make_plan(M, K, N, group, d->sms, d->smem_optin, zeros != nullptr);
   if (g.stages < 2 || g.units > 0x7FFFFFFFLL / 2) return MARLIN_ERR_UNSUPPORTED;
+  if (g.kind == kKernelTcgen05 && g.a_slots < 4) return MARLIN_ERR_UNSUPPORTED;
   if (workspace_bytes < g.ws_bytes) return MARLIN_ERR_WORKSPACE_TOO_SMALL;
 
   {
@@ -270,6 +278,8 @@ marlin_status_t marlin_gemm(const uint16_t* X, const void* packed, const uint16_
                (zeros ? kTileN / 2 : 0);
   p.weights_reused = g.m_tiles > 1;
   p.nacc = g.nacc > 0 ? g.nacc : 1;
+  p.a_slots = g.a_slots;
+  p.a_base = (uint32_t)(kTmemCols - g.a_slots * g.cpu * (kChunkK / 2));
   p.tx_w = (uint32_t)g.cpu * kChunkCodeBytes + (uint32_t)g.n_g * (kTileN * 2 + (zeros ? kTileN / 2 : 0));
   p.tx_x = (uint32_t)g.cpu * p.x_chunk_bytes;
   p.n_g = g.n_g;

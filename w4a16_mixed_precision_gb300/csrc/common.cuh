@@ -255,6 +255,29 @@ __device__ __forceinline__ void dequant_mma(float (&acc)[NB][4], uint32_t w, uin
   "mul.rn.f16x2 t2_" X ", t2_" X ", " S ";\n\t"                        \
   "mul.rn.f16x2 t3_" X ", t3_" X ", " S8 ";\n\t"
 
+// The same dequantisation into registers, in the store's register order, for
+// callers that store later (after waiting for a free tensor-memory slot).
+__device__ __forceinline__ void dequant16(uint4 w, uint32_t sub_r, uint32_t add_r8, uint32_t s_r,
+                                          uint32_t s_r8, uint32_t (&o)[16]) {
+  asm volatile(
+      "{\n\t.reg .b32 w8, k16, t0_0, t1_0, t2_0, t3_0, t0_1, t1_1, t2_1, t3_1, t0_2, t1_2, t2_2, "
+      "t3_2, t0_3, t1_3, t2_3, t3_3;\n\t"
+      "mov.b32 k16, 0x2C002C00;\n\t"
+      W4A16_DEQW_PTX("%16", "%20", "%21", "%22", "%23", "0")
+      W4A16_DEQW_PTX("%17", "%20", "%21", "%22", "%23", "1")
+      W4A16_DEQW_PTX("%18", "%20", "%21", "%22", "%23", "2")
+      W4A16_DEQW_PTX("%19", "%20", "%21", "%22", "%23", "3")
+      "mov.b32 %0, t0_0;\n\tmov.b32 %1, t2_0;\n\tmov.b32 %2, t1_0;\n\tmov.b32 %3, t3_0;\n\t"
+      "mov.b32 %4, t0_1;\n\tmov.b32 %5, t2_1;\n\tmov.b32 %6, t1_1;\n\tmov.b32 %7, t3_1;\n\t"
+      "mov.b32 %8, t0_2;\n\tmov.b32 %9, t2_2;\n\tmov.b32 %10, t1_2;\n\tmov.b32 %11, t3_2;\n\t"
+      "mov.b32 %12, t0_3;\n\tmov.b32 %13, t2_3;\n\tmov.b32 %14, t1_3;\n\tmov.b32 %15, t3_3;\n\t"
+      "}"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3]), "=r"(o[4]), "=r"(o[5]), "=r"(o[6]),
+        "=r"(o[7]), "=r"(o[8]), "=r"(o[9]), "=r"(o[10]), "=r"(o[11]), "=r"(o[12]), "=r"(o[13]),
+        "=r"(o[14]), "=r"(o[15])
+      : "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w), "r"(sub_r), "r"(add_r8), "r"(s_r), "r"(s_r8));
+}
+
 __device__ __forceinline__ void dequant_store_tmem(uint32_t taddr, uint4 w, uint32_t sub_r,
                                                    uint32_t add_r8, uint32_t s_r, uint32_t s_r8) {
   asm volatile(

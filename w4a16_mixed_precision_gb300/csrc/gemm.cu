@@ -53,7 +53,6 @@ constexpr int kNumDqWG = 4;                // dequant warpgroups
 constexpr int kNumDqWarps = 4 * kNumDqWG;
 constexpr int kFirstDqWarp = 4;
 static_assert((kNumDqWG & (kNumDqWG - 1)) == 0, "unit residues need a power-of-two warpgroup count");
-static_assert((kAStages / 2) % kNumDqWG == 0, "A slots must be a multiple of the warpgroup count");
 static_assert(kThreads == 32 * (kFirstDqWarp + kNumDqWarps), "block size");
 
 // ---- the kernel -----------------------------------------------------------------
@@ -190,18 +189,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_drain(bar(ctrl->full[i % S]), (uint32_t)((i / S) & 1), wc);
     }
   } else if (warp == 1 || warp == 2) {
-    // ================= MMA issuers (one thread each) =================
+    // ================= MMA issuers (one warp each) =================
     // With two issuers, issuer i takes the units i, i+2, ... of the stripe into
     // its own accumulator; with one, every unit.  Every barrier ring is indexed
     // by the stripe's unit index, and each consumer of a ring takes a fixed
     // residue of it (issuer: unit mod 2, dequant warpgroup: unit mod 4; the
-    // stage count and the A slots are multiples of 4), so a consumer is never
-    // more than one phase ahead of a barrier it waits on.
+    // stage count is a multiple of 4; the A slot count is even and at least 4,
+    // and each issuer's MMAs complete in order), so a consumer is never more
+    // than one phase ahead of a barrier it waits on.
+    // The whole warp runs the loop; one elected lane issues each MMA and commit.
     const int iss = warp - 1;
-    if (lane == 0 && iss < nacc) {
+    if (iss < nacc) {
       const uint32_t idesc = umma_idesc_f16_f32((uint32_t)p.bn);
       const uint32_t d_tmem = tmem + (uint32_t)(iss * p.bn);
-      const int a_slots = kAStages / cpu;
+      const int a_slots = p.a_slots;
       const uint32_t a_cols = (uint32_t)cpu * (kChunkK / 2);
       int s = 0, a = 0, seg = 0;
       uint32_t ph = 0, aph = 0;
@@ -210,43 +211,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ok && u < u_end) {
         const int seg_len = min(u_end - u, KT - ku);
         if (seg > 0) {
-          if (!wait_thread(bar(ctrl->dempty), (uint32_t)((seg - 1) & 1), wc)) break;
+          if (!wait_warp(bar(ctrl->dempty), (uint32_t)((seg - 1) & 1), wc)) break;
           tc_fence_after();
         }
         uint32_t acc = 0;
         for (int i = 0; i < seg_len; ++i) {
           if (((u - u_begin + i) & (nacc - 1)) == iss) {
-            if (!wait_thread(bar(ctrl->full[s]), ph, wc)) { ok = false; break; }
-            if (!wait_thread(bar(ctrl->afull[a]), aph, wc)) { ok = false; break; }
+            // the unit's A slot is filled only after its dequant warpgroup saw
+            // the stage land, so its completion also covers the X tiles
+            if (!wait_warp(bar(ctrl->afull[a]), aph, wc)) { ok = false; break; }
             tc_fence_after();
             const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
-            const uint32_t a_col = tmem + kAColBase + (uint32_t)a * a_cols;
+            const uint32_t a_col = tmem + p.a_base + (uint32_t)a * a_cols;
             for (int j = 0; j < cpu; ++j) {
               const uint64_t desc0 = umma_desc_sw128(st + (uint32_t)j * p.x_chunk_bytes);
 #pragma unroll
               for (int kk = 0; kk < kChunkK / 16; ++kk) {
                 // +32 bytes per 16-row step = +2 in the descriptor's address field
-                mma_f16_ts(d_tmem, a_col + (uint32_t)(j * (kChunkK / 2) + kk * 8),
+                mma_f16_ts_elect(d_tmem, a_col + (uint32_t)(j * (kChunkK / 2) + kk * 8),
                            desc0 + (uint64_t)(2 * kk), idesc, acc);
                 acc = 1;
               }
             }
-            mma_commit(bar(ctrl->aempty[a]));
-            mma_commit(bar(ctrl->empty[s]));
+            mma_commit_elect(bar(ctrl->aempty[a]));
+            mma_commit_elect(bar(ctrl->empty[s]));
           }
           if (++a == a_slots) { a = 0; aph ^= 1u; }
           if (++s == S) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
         // an issuer without a unit in this segment has nothing in flight for it
-        if (acc) mma_commit(bar(ctrl->dfull));
-        else mbar_arrive(bar(ctrl->dfull));
+        if (acc) mma_commit_elect(bar(ctrl->dfull));
+        else if (lane == 0) mbar_arrive(bar(ctrl->dfull));
         ++seg;
         u += seg_len;
         ku = 0;
       }
       // Every issued MMA must finish before TMEM is released.
-      mma_commit(bar(ctrl->drain[iss]));
+      mma_commit_elect(bar(ctrl->drain[iss]));
       wait_drain(bar(ctrl->drain[iss]), 0, wc);
     }
   } else if (warp >= kFirstDqWarp) {
@@ -264,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sc_off = p.off_scales + (uint32_t)c0 * 2;
     const uint32_t zr_off = p.off_zeros + (uint32_t)(c0 >> 1);
     const uint32_t z_shift = (uint32_t)(c0 & 1) * 4;
-    const int a_slots = kAStages / cpu;
+    const int a_slots = p.a_slots;
     const uint32_t a_cols = (uint32_t)cpu * (kChunkK / 2);
     int s = 0, a = 0, seg = 0;
     uint32_t ph = 0, aph = 0;
@@ -280,13 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_warp(bar(ctrl->full[s]), ph, wc)) { ok = false; break; }
           const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
           // a unit (cpu <= 2 chunks of 64 rows, group >= 128) lies in one group row
-          uint4 w0[2], w1[2];
-#pragma unroll
-          for (int j = 0; j < 2; ++j)
-            if (j < cpu) {
-              w0[j] = lds128(st + code_off + (uint32_t)j * kChunkCodeBytes);        // group 2q
-              w1[j] = lds128(st + code_off + (uint32_t)j * kChunkCodeBytes + 512);  // group 2q+1
-            }
+          const uint4 w0 = lds128(st + code_off);        // chunk 0, group 2q
+          const uint4 w1 = lds128(st + code_off + 512);  // chunk 0, group 2q+1
           uint32_t z0 = 8, z1 = 8, z2 = 8, z3 = 8;
           if (has_zeros) {
             z0 = (lds_u8(st + zr_off) >> z_shift) & 0xFu;
@@ -298,19 +295,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           const ColConst k1 = col_const((uint16_t)lds_u16(st + sc_off + 16), z1);
           const ColConst k2 = col_const((uint16_t)lds_u16(st + sc_off + 32), z2);
           const ColConst k3 = col_const((uint16_t)lds_u16(st + sc_off + 48), z3);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(ctrl->empty[s]));
-
+          // the first chunk is dequantised before waiting for the slot, so that
+          // only its stores sit between the slot's release and its refill
+          uint32_t d0[16], d1[16];
+          dequant16(w0, k0.sub, k1.add, k0.s, k1.s, d0);
+          dequant16(w1, k2.sub, k3.add, k2.s, k3.s, d1);
           if (!wait_warp(bar(ctrl->aempty[a]), aph ^ 1u, wc)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t acol = tmem + kAColBase + (uint32_t)a * a_cols + lane_off;
-#pragma unroll
-          for (int j = 0; j < 2; ++j)
-            if (j < cpu) {
-              const uint32_t cj = acol + (uint32_t)j * (kChunkK / 2);
-              dequant_store_tmem(cj, w0[j], k0.sub, k1.add, k0.s, k1.s);
-              dequant_store_tmem(cj + (16u << 16), w1[j], k2.sub, k3.add, k2.s, k3.s);
-            }
+          const uint32_t acol = tmem + p.a_base + (uint32_t)a * a_cols + lane_off;
+          tmem_st_16x256b_x4(acol, d0);
+          tmem_st_16x256b_x4(acol + (16u << 16), d1);
+          if (cpu == 2) {
+            const uint4 v0 = lds128(st + code_off + kChunkCodeBytes);
+            const uint4 v1 = lds128(st + code_off + kChunkCodeBytes + 512);
+            const uint32_t c1 = acol + (uint32_t)(kChunkK / 2);
+            dequant_store_tmem(c1, v0, k0.sub, k1.add, k0.s, k1.s);
+            dequant_store_tmem(c1 + (16u << 16), v1, k2.sub, k3.add, k2.s, k3.s);
+          }
+          // codes and scales read: the stage may be refilled once the MMA is done too
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(ctrl->empty[s]));
           tmem_wait_st();
           tc_fence_before();
           __syncwarp();

@@ -13,9 +13,8 @@ constexpr int kThreads = 640;      // 20 warps: 2 producers, 2 MMA issuers (one 
 constexpr int kTileN = 128;        // output columns per tile = UMMA M
 constexpr int kChunkK = 64;        // K elements per dequantised A chunk
 constexpr int kChunkCodeBytes = kTileN * kChunkK / 2;  // 4096
-constexpr int kAStages = 8;        // A chunks resident in TMEM
+constexpr int kAStages = 12;       // most A slots (one unit each) resident in TMEM
 constexpr int kTmemCols = 512;
-constexpr int kAColBase = 256;     // TMEM column of A stage 0; D lives in columns [0, 256)
 constexpr int kMaxStages = 16;
 constexpr int kCtrlBytes = 1024;   // barriers and flags at the front of dynamic smem
 constexpr int kMaxBn = 256;        // tokens per m-tile (UMMA N)
@@ -48,6 +47,8 @@ struct GemmParams {
   int n_g;                  // scale/zero group rows per unit (2 only for group 128, 256-row units)
   int units_per_group;      // units per group row (>= 1)
   uint32_t off_xchg;        // small-M kernel: exchange buffer, bytes after stage 0
+  int a_slots;              // tcgen05 kernel: A slots in TMEM (even, >= 4, <= kAStages)
+  uint32_t a_base;          // tcgen05 kernel: TMEM column of A slot 0 (accumulators below it)
   unsigned long long timeout_ns;
 };
 
@@ -55,7 +56,7 @@ struct GemmParams {
 enum KernelKind { kKernelTcgen05 = 0, kKernelSmallM = 1 };
 struct GemmPlan {
   int kind;
-  int bn, m_tiles, n_tiles, kt, cpu, stages, grid, n_g, upg, nacc;
+  int bn, m_tiles, n_tiles, kt, cpu, stages, grid, n_g, upg, nacc, a_slots;
   uint32_t off_xchg;
   long long units;
   uint32_t stage_bytes, smem_bytes;
