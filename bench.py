@@ -72,6 +72,14 @@ def kernel_source_digest() -> str:
     return h.hexdigest()[:16]
 
 
+def kernel_names(problems) -> str:
+    """The fused kernels a workload launches: the warp-level path for M <= 24,
+    the tcgen05 path above (the library's default split)."""
+    small = any(p.M <= 24 for p in problems)
+    big = any(p.M > 24 for p in problems)
+    return " + ".join(n for n, on in (("w4a16_small_m_kernel", small), ("w4a16_gemm_kernel", big)) if on)
+
+
 def recorded_traffic(workload: str):
     """dram bytes per launch from a committed ncu capture, if the kernel sources
     have not changed since it was taken; else None."""
@@ -265,7 +273,7 @@ def run_reference(args, problems, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_s / max(args.steps, 1) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD_NAMES[args.workload]},
+            "config": {"workload": WORKLOAD_NAMES.get(args.workload, args.workload)},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -402,7 +410,7 @@ def run_gpu(args, problems, rank, world, local):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": WORKLOAD_NAMES[args.workload],
+        "config": {"workload": WORKLOAD_NAMES.get(args.workload, args.workload),
                    "problems_per_step": launches, "graph_phases": P,
                    "l2": f"inputs larger than L2: rotating weight copies ({weight_copies_bytes / 1e6:.0f} MB "
                          f"in all), each read once per {P} step(s), so no call finds its weights in L2",
@@ -413,7 +421,7 @@ def run_gpu(args, problems, rank, world, local):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(args.workload),
                      "peak_source": peaks["source"],
-                     "kernel": "w4a16_gemm_kernel (every launch of the step)",
+                     "kernel": kernel_names(problems) + " (every launch of the step)",
                      "bytes_per_launch": step_bytes / launches,
                      "avg_launch_us": ms_per_step * 1e3 / launches},
         "clocks": clocks,
@@ -425,7 +433,7 @@ def run_gpu(args, problems, rank, world, local):
         line["roofline"] = {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
                             "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"], "traffic": None,
                             "peak_source": peaks["source"] + " bf16 (fp16 dense rate is the same)",
-                            "kernel": "w4a16_gemm_kernel"}
+                            "kernel": kernel_names(problems)}
     if rank == 0 and not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
         v, s, desc = oracle_baseline(problems, args.cpu_budget, threads)
@@ -534,9 +542,16 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     ap.add_argument("--no-soak", action="store_true", help="skip the 1 s clock soak (profiling)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--shape", default=None,
+                    help="one problem M,K,N[,group[,asym]] instead of a workload (profiling a single kernel)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     problems = ALL_CONFIGS[args.workload]
+    if args.shape:
+        v = [int(t) for t in args.shape.split(",")]
+        M, K, N = v[0], v[1], v[2]
+        problems = [Problem("shape", M, K, N, v[3] if len(v) > 3 else 128, bool(v[4]) if len(v) > 4 else False)]
+        args.workload = f"shape {M}x{K}x{N}"
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
         run_reference(args, problems, rank, int(os.environ.get("WORLD_SIZE", "1")))

@@ -34,6 +34,8 @@ SMALL_CASES = [
     (5, 256, 384, 128, True),
     (16, 1024, 512, 128, False),
     (17, 512, 256, 128, True),
+    (24, 1024, 640, 128, False),       # largest batch of the warp-level kernel by default
+    (25, 1024, 640, 128, True),        # smallest batch of the tcgen05 kernel by default
     (32, 2048, 1024, 128, False),
     (33, 1024, 640, 1024, True),       # one scale per column, ragged M
     (48, 2048, 768, 128, True),

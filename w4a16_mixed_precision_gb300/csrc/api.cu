@@ -68,10 +68,14 @@ bool valid_shape(int K, int N) { return K > 0 && N > 0 && K % 128 == 0 && N % 12
 
 // Largest M served by the small-batch kernel (mma.sync path); larger M uses the
 // tcgen05 kernel.  W4A16_SMALL_M_MAX overrides it (0 disables the small path).
+// Largest M served by the warp-level kernel (measured crossover: at M = 32 the
+// tcgen05 kernel is faster on every decode shape, at M <= 24 the warp-level
+// one).  W4A16_SMALL_M_MAX overrides it (0..32), e.g. to test either kernel at
+// any M.
 int small_m_max() {
   static int v = [] {
     const char* e = getenv("W4A16_SMALL_M_MAX");
-    int x = e ? atoi(e) : 32;
+    int x = e ? atoi(e) : 24;
     return x < 0 ? 0 : (x > 32 ? 32 : x);
   }();
   return v;

@@ -1,4 +1,5 @@
-// small_m.cu -- the fused W4A16 matrix multiply for small batches (M <= 32):
+// small_m.cu -- the fused W4A16 matrix multiply for small batches (M <= 32; by
+// default the library sends M <= 24 here and larger batches to gemm.cu):
 // Y[M][N] = X[M][K] . dequant(W)[K][N] on the warp-level tensor-core path.
 //
 // At M <= 32 the multiply is bound by streaming the 4-bit weights from HBM, and
