@@ -104,13 +104,17 @@ GemmPlan make_plan(int M, int K, int N, int group, int sms, int smem_optin, bool
     // two MMA issuers (accumulators of bn columns each, one per dequant
     // warpgroup and 64-row chunk of a 128-row unit) when both fit beside the A
     // stages in tensor memory
-    g.nacc = g.bn <= 128 ? 2 : 1;
-    g.cpu = g.nacc == 2 ? 2 : 1;
+    // two MMA issuers: for bn <= 128 on alternate units, each into its own
+    // accumulator; above, on every unit, splitting the bn token columns of one
+    // accumulator at 128 (so each issues MMAs of N <= 128)
+    g.nacc = 2;
+    g.split_n = g.bn > 128 ? 1 : 0;
+    g.cpu = g.split_n ? 1 : 2;
     // A slots (one unit of cpu*64 rows = cpu*32 columns each) fill the tensor
     // memory above the accumulators; an even count of at least 4 keeps every
     // waiter within one phase of the slot barriers
     const int a_cols = g.cpu * kChunkK / 2;
-    int slots = (kTmemCols - g.nacc * g.bn) / a_cols;
+    int slots = (kTmemCols - (g.split_n ? 1 : g.nacc) * g.bn) / a_cols;
     if (slots > kAStages) slots = kAStages;
     g.a_slots = slots & ~1;
   }
@@ -126,8 +130,12 @@ GemmPlan make_plan(int M, int K, int N, int group, int sms, int smem_optin, bool
   const size_t xchg = g.kind == kKernelSmallM ? (size_t)4 * (g.bn / 8) * 256 * sizeof(float) : 0;
   int stages = (int)((budget - (long long)xchg) / (long long)g.stage_bytes);
   if (stages > kMaxStages) stages = kMaxStages;
-  // tcgen05 kernel: each consumer takes a fixed residue of the unit index mod 4
-  if (g.kind == kKernelTcgen05) stages &= ~3;
+  // tcgen05 kernel: each dequant warpgroup takes a fixed residue of the unit
+  // index mod 4.  With a stage count that is a multiple of 4 a warpgroup only
+  // waits on its own stages; the large-bn plan keeps every stage that fits
+  // (its X tiles make stages big) and has the warpgroups wait on every
+  // stage's phase instead.
+  if (g.kind == kKernelTcgen05 && !g.split_n) stages &= ~3;
   g.stages = stages;
   g.off_xchg = (uint32_t)((size_t)stages * g.stage_bytes);
   g.smem_bytes = (uint32_t)(kCtrlBytes + 1024 + (size_t)stages * g.stage_bytes + xchg);
@@ -282,6 +290,8 @@ marlin_status_t marlin_gemm(const uint16_t* X, const void* packed, const uint16_
                (zeros ? kTileN / 2 : 0);
   p.weights_reused = g.m_tiles > 1;
   p.nacc = g.nacc > 0 ? g.nacc : 1;
+  p.split_n = g.split_n;
+  p.full_all = (g.stages % 4) != 0;
   p.a_slots = g.a_slots;
   p.a_base = (uint32_t)(kTmemCols - g.a_slots * g.cpu * (kChunkK / 2));
   p.tx_w = (uint32_t)g.cpu * kChunkCodeBytes + (uint32_t)g.n_g * (kTileN * 2 + (zeros ? kTileN / 2 : 0));

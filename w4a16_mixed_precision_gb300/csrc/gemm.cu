@@ -91,11 +91,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(bar(ctrl->full[s]), 2);                 // weights + activation producers
-      mbar_init(bar(ctrl->empty[s]), 4 + 1);            // one dequant warpgroup + one MMA issuer
+      // the unit's dequant warpgroup (every dequant warp when they all track
+      // every stage) and its MMA issuer(s)
+      mbar_init(bar(ctrl->empty[s]), (p.full_all ? kNumDqWarps : 4) + (p.split_n ? 2 : 1));
     }
     for (int a = 0; a < kAStages; ++a) {
       mbar_init(bar(ctrl->afull[a]), 4);
-      mbar_init(bar(ctrl->aempty[a]), 1);
+      mbar_init(bar(ctrl->aempty[a]), p.split_n ? 2 : 1);
     }
     mbar_init(bar(ctrl->dfull), nacc);
     mbar_init(bar(ctrl->dempty), kNumDqWarps);
@@ -190,18 +192,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1 || warp == 2) {
     // ================= MMA issuers (one warp each) =================
-    // With two issuers, issuer i takes the units i, i+2, ... of the stripe into
-    // its own accumulator; with one, every unit.  Every barrier ring is indexed
+    // For bn <= 128, issuer i takes the units i, i+2, ... of the stripe into
+    // its own accumulator.  For bn > 128 (split_n), both take every unit:
+    // issuer 0 the token columns [0, 128) of the accumulator, issuer 1 the
+    // columns [128, bn), each with MMAs of N <= 128 reading its rows of X.  Every barrier ring is indexed
     // by the stripe's unit index, and each consumer of a ring takes a fixed
     // residue of it (issuer: unit mod 2, dequant warpgroup: unit mod 4; the
-    // stage count is a multiple of 4; the A slot count is even and at least 4,
-    // and each issuer's MMAs complete in order), so a consumer is never more
-    // than one phase ahead of a barrier it waits on.
+    // stage count is a multiple of 4 or the warpgroups wait on every stage;
+    // the A slot count is even and at least 4, and each issuer's MMAs complete
+    // in order), so a consumer is never more than one phase ahead of a barrier
+    // it waits on.
     // The whole warp runs the loop; one elected lane issues each MMA and commit.
     const int iss = warp - 1;
     if (iss < nacc) {
-      const uint32_t idesc = umma_idesc_f16_f32((uint32_t)p.bn);
-      const uint32_t d_tmem = tmem + (uint32_t)(iss * p.bn);
+      const bool split = p.split_n != 0;
+      const uint32_t n_iss = split ? (iss == 0 ? 128u : (uint32_t)p.bn - 128u) : (uint32_t)p.bn;
+      const uint32_t idesc = umma_idesc_f16_f32(n_iss);
+      const uint32_t d_tmem = tmem + (uint32_t)(split ? iss * 128 : iss * p.bn);
+      const uint32_t x_rows = split ? (uint32_t)(iss * 128 * 128) : 0u;  // bytes: 128 rows of 128 B
       const int a_slots = p.a_slots;
       const uint32_t a_cols = (uint32_t)cpu * (kChunkK / 2);
       int s = 0, a = 0, seg = 0;
@@ -216,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint32_t acc = 0;
         for (int i = 0; i < seg_len; ++i) {
-          if (((u - u_begin + i) & (nacc - 1)) == iss) {
+          if (split || ((u - u_begin + i) & (nacc - 1)) == iss) {
             // the unit's A slot is filled only after its dequant warpgroup saw
             // the stage land, so its completion also covers the X tiles
             if (!wait_warp(bar(ctrl->afull[a]), aph, wc)) { ok = false; break; }
@@ -224,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
             const uint32_t a_col = tmem + p.a_base + (uint32_t)a * a_cols;
             for (int j = 0; j < cpu; ++j) {
-              const uint64_t desc0 = umma_desc_sw128(st + (uint32_t)j * p.x_chunk_bytes);
+              const uint64_t desc0 = umma_desc_sw128(st + (uint32_t)j * p.x_chunk_bytes + x_rows);
 #pragma unroll
               for (int kk = 0; kk < kChunkK / 16; ++kk) {
                 // +32 bytes per 16-row step = +2 in the descriptor's address field
@@ -278,7 +286,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nt = tile - mt * p.n_tiles;
       // ---- mainloop: dequantise this warpgroup's units into TMEM ----
       for (int i = 0; i < seg_len; ++i) {
-        if (((u - u_begin + i) & (kNumDqWG - 1)) == wg) {
+        const bool mine = ((u - u_begin + i) & (kNumDqWG - 1)) == wg;
+        if (!mine && p.full_all) {
+          // track every stage: wait for it and release it, so that the ring can
+          // neither run a phase ahead of this warp nor lap it
+          if (!wait_warp(bar(ctrl->full[s]), ph, wc)) { ok = false; break; }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(ctrl->empty[s]));
+        }
+        if (mine) {
           if (!wait_warp(bar(ctrl->full[s]), ph, wc)) { ok = false; break; }
           const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
           // a unit (cpu <= 2 chunks of 64 rows, group >= 128) lies in one group row
@@ -350,8 +366,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float* part = p.partials + (size_t)blockIdx.x * ((size_t)p.bn * kTileN);
       // accumulators holding units of this tile: both, or the one of its only unit
-      const bool two = nacc == 2 && seg_len >= 2;
-      const uint32_t d_first = (nacc == 2 && seg_len == 1) ? (uint32_t)(((u - u_begin) & 1) * p.bn) : 0u;
+      const bool alt = nacc == 2 && !p.split_n;
+      const bool two = alt && seg_len >= 2;
+      const uint32_t d_first = (alt && seg_len == 1) ? (uint32_t)(((u - u_begin) & 1) * p.bn) : 0u;
       for (int cc = wg; cc < p.bn / 8; cc += kNumDqWG) {
         uint32_t r[8], r1[8];
         tmem_ld_x8(tmem + lane_off + d_first + (uint32_t)cc * 8, r);

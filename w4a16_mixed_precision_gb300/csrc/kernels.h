@@ -43,6 +43,9 @@ struct GemmParams {
   uint32_t tx_bytes;        // bytes landed per stage
   int weights_reused;       // more than one m-tile reads the same weights
   int nacc;                 // tcgen05 kernel: MMA issuers, each with its own accumulator (1 or 2)
+  int full_all;             // tcgen05 kernel: dequant warps wait on every stage (stage count not a multiple of 4)
+  int split_n;              // tcgen05 kernel, bn > 128: the two issuers take token columns
+                            // [0, 128) and [128, bn) of every unit (one accumulator of bn columns)
   uint32_t tx_w, tx_x;      // bytes landed per stage by the weights / activation producer
   int n_g;                  // scale/zero group rows per unit (2 only for group 128, 256-row units)
   int units_per_group;      // units per group row (>= 1)
@@ -56,7 +59,7 @@ struct GemmParams {
 enum KernelKind { kKernelTcgen05 = 0, kKernelSmallM = 1 };
 struct GemmPlan {
   int kind;
-  int bn, m_tiles, n_tiles, kt, cpu, stages, grid, n_g, upg, nacc, a_slots;
+  int bn, m_tiles, n_tiles, kt, cpu, stages, grid, n_g, upg, nacc, a_slots, split_n;
   uint32_t off_xchg;
   long long units;
   uint32_t stage_bytes, smem_bytes;
