@@ -109,7 +109,7 @@ GemmPlan make_plan(int M, int K, int N, int group, int sms, int smem_optin, bool
     // accumulator at 128 (so each issues MMAs of N <= 128)
     g.nacc = 2;
     g.split_n = g.bn > 128 ? 1 : 0;
-    g.cpu = g.split_n ? 1 : 2;
+    g.cpu = 2;
     // A slots (one unit of cpu*64 rows = cpu*32 columns each) fill the tensor
     // memory above the accumulators; an even count of at least 4 keeps every
     // waiter within one phase of the slot barriers
