@@ -132,10 +132,11 @@ GemmPlan make_plan(int M, int K, int N, int group, int sms, int smem_optin, bool
   if (stages > kMaxStages) stages = kMaxStages;
   // tcgen05 kernel: each dequant warpgroup takes a fixed residue of the unit
   // index mod 4.  With a stage count that is a multiple of 4 a warpgroup only
-  // waits on its own stages; the large-bn plan keeps every stage that fits
-  // (its X tiles make stages big) and has the warpgroups wait on every
-  // stage's phase instead.
-  if (g.kind == kKernelTcgen05 && !g.split_n) stages &= ~3;
+  // waits on its own stages.  Where rounding down would cost a large share of
+  // a short ring (big X tiles at large bn), every stage that fits is kept and
+  // the warpgroups track every stage's phase instead (measured: faster for
+  // rings of 3..7 stages, slower for 9 -> 8).
+  if (g.kind == kKernelTcgen05 && stages >= 8) stages &= ~3;
   g.stages = stages;
   g.off_xchg = (uint32_t)((size_t)stages * g.stage_bytes);
   g.smem_bytes = (uint32_t)(kCtrlBytes + 1024 + (size_t)stages * g.stage_bytes + xchg);
