@@ -292,6 +292,7 @@ marlin_status_t marlin_gemm(const uint16_t* X, const void* packed, const uint16_
   p.weights_reused = g.m_tiles > 1;
   p.nacc = g.nacc > 0 ? g.nacc : 1;
   p.split_n = g.split_n;
+  p.split_h = g.bn > 128 ? 128 : (int)round_up((size_t)(g.bn / 2), 16);
   p.full_all = (g.stages % 4) != 0;
   p.a_slots = g.a_slots;
   p.a_base = (uint32_t)(kTmemCols - g.a_slots * g.cpu * (kChunkK / 2));

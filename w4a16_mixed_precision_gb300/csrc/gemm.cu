@@ -206,46 +206,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int iss = warp - 1;
     if (iss < nacc) {
       const bool split = p.split_n != 0;
-      const uint32_t n_iss = split ? (iss == 0 ? 128u : (uint32_t)p.bn - 128u) : (uint32_t)p.bn;
+      const uint32_t sh = (uint32_t)p.split_h;
+      const uint32_t n_iss = split ? (iss == 0 ? sh : (uint32_t)p.bn - sh) : (uint32_t)p.bn;
       const uint32_t idesc = umma_idesc_f16_f32(n_iss);
-      const uint32_t d_tmem = tmem + (uint32_t)(split ? iss * 128 : iss * p.bn);
-      const uint32_t x_rows = split ? (uint32_t)(iss * 128 * 128) : 0u;  // bytes: 128 rows of 128 B
+      const uint32_t d_tmem = tmem + (split ? (uint32_t)iss * sh : (uint32_t)(iss * p.bn));
+      const uint32_t x_rows = split ? (uint32_t)iss * sh * 128u : 0u;  // bytes: sh rows of 128 B
       const int a_slots = p.a_slots;
       const uint32_t a_cols = (uint32_t)cpu * (kChunkK / 2);
+      // this issuer's units are r = first, first + stride, ... (r = unit index
+      // in the stripe); (s, a) is the ring position of unit r
+      const int stride = split ? 1 : nacc;
       int s = 0, a = 0, seg = 0;
       uint32_t ph = 0, aph = 0;
+      auto advance = [&](int n) {
+        s += n;
+        while (s >= S) { s -= S; ph ^= 1u; }
+        a += n;
+        while (a >= a_slots) { a -= a_slots; aph ^= 1u; }
+      };
+      int r = split ? 0 : iss;
+      advance(r);
       int u = u_begin, ku = ku_begin;
       bool ok = true;
       while (ok && u < u_end) {
         const int seg_len = min(u_end - u, KT - ku);
+        const int r_end = u - u_begin + seg_len;  // first unit of the next segment
         if (seg > 0) {
           if (!wait_warp(bar(ctrl->dempty), (uint32_t)((seg - 1) & 1), wc)) break;
           tc_fence_after();
         }
         uint32_t acc = 0;
-        for (int i = 0; i < seg_len; ++i) {
-          if (split || ((u - u_begin + i) & (nacc - 1)) == iss) {
-            // the unit's A slot is filled only after its dequant warpgroup saw
-            // the stage land, so its completion also covers the X tiles
-            if (!wait_warp(bar(ctrl->afull[a]), aph, wc)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
-            const uint32_t a_col = tmem + p.a_base + (uint32_t)a * a_cols;
-            for (int j = 0; j < cpu; ++j) {
-              const uint64_t desc0 = umma_desc_sw128(st + (uint32_t)j * p.x_chunk_bytes + x_rows);
+        for (; r < r_end; r += stride) {
+          // the unit's A slot is filled only after its dequant warpgroup saw
+          // the stage land, so its completion also covers the X tiles
+          if (!wait_warp(bar(ctrl->afull[a]), aph, wc)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
+          const uint32_t a_col = tmem + p.a_base + (uint32_t)a * a_cols;
+          for (int j = 0; j < cpu; ++j) {
+            const uint64_t desc0 = umma_desc_sw128(st + (uint32_t)j * p.x_chunk_bytes + x_rows);
 #pragma unroll
-              for (int kk = 0; kk < kChunkK / 16; ++kk) {
-                // +32 bytes per 16-row step = +2 in the descriptor's address field
-                mma_f16_ts_elect(d_tmem, a_col + (uint32_t)(j * (kChunkK / 2) + kk * 8),
-                           desc0 + (uint64_t)(2 * kk), idesc, acc);
-                acc = 1;
-              }
+            for (int kk = 0; kk < kChunkK / 16; ++kk) {
+              // +32 bytes per 16-row step = +2 in the descriptor's address field
+              mma_f16_ts_elect(d_tmem, a_col + (uint32_t)(j * (kChunkK / 2) + kk * 8),
+                               desc0 + (uint64_t)(2 * kk), idesc, acc);
+              acc = 1;
             }
-            mma_commit_elect(bar(ctrl->aempty[a]));
-            mma_commit_elect(bar(ctrl->empty[s]));
           }
-          if (++a == a_slots) { a = 0; aph ^= 1u; }
-          if (++s == S) { s = 0; ph ^= 1u; }
+          mma_commit_elect(bar(ctrl->aempty[a]));
+          mma_commit_elect(bar(ctrl->empty[s]));
+          advance(stride);
         }
         if (!ok) break;
         // an issuer without a unit in this segment has nothing in flight for it

@@ -43,6 +43,7 @@ struct GemmParams {
   uint32_t tx_bytes;        // bytes landed per stage
   int weights_reused;       // more than one m-tile reads the same weights
   int nacc;                 // tcgen05 kernel: MMA issuers, each with its own accumulator (1 or 2)
+  int split_h;              // split_n: token columns of the first issuer (multiple of 16)
   int full_all;             // tcgen05 kernel: dequant warps wait on every stage (stage count not a multiple of 4)
   int split_n;              // tcgen05 kernel, bn > 128: the two issuers take token columns
                             // [0, 128) and [128, bn) of every unit (one accumulator of bn columns)
