@@ -499,24 +499,42 @@ def per_run_table(problems, packed, ws, xs, ys, dev, peaks):
 
 
 def end_to_end(problems, packed, ws, plans, dev, args, step_bytes):
+    """The step through the public API with host buffers: every step copies all
+    of its activations in from pinned host memory (one copy of one buffer that
+    holds every problem's X), makes the 24 marlin_gemm calls (gemm_into), and
+    copies every Y back (one copy), on one stream."""
     import torch
 
     import w4a16_mixed_precision_gb300 as w4
-    hx = [torch.from_numpy(make_activations(p.M, p.K, seed_for(p.key))).pin_memory() for p in problems]
-    hy = [torch.empty((p.M, p.N), dtype=torch.float16).pin_memory() for p in problems]
-    dx = [torch.empty((p.M, p.K), dtype=torch.float16, device=dev) for p in problems]
-    dy = [torch.empty((p.M, p.N), dtype=torch.float16, device=dev) for p in problems]
-    h2d = sum(t.numel() * 2 for t in hx)
-    d2h = sum(t.numel() * 2 for t in hy)
+    xs_n = [p.M * p.K for p in problems]
+    ys_n = [p.M * p.N for p in problems]
+
+    def offsets(ns):  # 16-byte aligned element offsets
+        out, o = [], 0
+        for n in ns:
+            out.append(o)
+            o += (n + 7) // 8 * 8
+        return out, o
+
+    xo, xt = offsets(xs_n)
+    yo, yt = offsets(ys_n)
+    hx = torch.empty(xt, dtype=torch.float16).pin_memory()
+    hy = torch.empty(yt, dtype=torch.float16).pin_memory()
+    for p, o, n in zip(problems, xo, xs_n):
+        hx[o:o + n].copy_(torch.from_numpy(make_activations(p.M, p.K, seed_for(p.key)).reshape(-1)))
+    dxb = torch.empty(xt, dtype=torch.float16, device=dev)
+    dyb = torch.empty(yt, dtype=torch.float16, device=dev)
+    dx = [dxb[o:o + n].view(p.M, p.K) for p, o, n in zip(problems, xo, xs_n)]
+    dy = [dyb[o:o + n].view(p.M, p.N) for p, o, n in zip(problems, yo, ys_n)]
     steps = max(3, min(args.steps, 200))
 
     def one(plan):
+        dxb.copy_(hx, non_blocking=True)
         for i, c in plan:
             p = problems[i]
             lk = (p.K, p.N, p.group, p.asym)
-            dx[i].copy_(hx[i], non_blocking=True)
             w4.gemm_into(dx[i], packed[lk][c], ws[lk], dy[i])
-            hy[i].copy_(dy[i], non_blocking=True)
+        hy.copy_(dyb, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
     for k in range(3):
@@ -525,9 +543,11 @@ def end_to_end(problems, packed, ws, plans, dev, args, step_bytes):
     for k in range(steps):
         one(plans[k % len(plans)])
     dt = (time.perf_counter() - t0) / steps
-    return {"value": step_bytes / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3, "steps": steps,
-            "path": "marlin_gemm via the Python binding, pinned host X in, Y out, per call"}
+    return {"value": step_bytes / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": xt * 2,
+            "d2h_bytes_per_step": yt * 2, "ms_per_step": dt * 1e3, "steps": steps,
+            "path": "per step: one H2D copy of all activations from pinned host memory, the 24 "
+                    "marlin_gemm calls through the Python binding, one D2H copy of all outputs; "
+                    "host wall clock around the whole step, synchronised"}
 
 
 def main():

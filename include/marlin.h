@@ -162,6 +162,28 @@ marlin_status_t marlin_gemm_no_alloc(const uint16_t* X, const void* packed, cons
                                      int group, marlin_stream_t stream);
 
 /*
+ * marlin_gemm with X and Y in host memory, as an inference loop that keeps
+ * activations on the host would call it.  The pages give no host-buffer form
+ * of the call; this one only adds the two copies around marlin_gemm.
+ *
+ * On `stream`, in order: copy X_host (fp16 [M][K], M*K*2 bytes) into X_dev,
+ * run marlin_gemm(X_dev, ..., Y_dev, ...), copy Y_dev (fp16 [M][N]) into
+ * Y_host.  One cudaMemcpyAsync per copy.
+ * X_host, Y_host  host; page-locked memory keeps the copies asynchronous
+ *                 (pageable memory works but the copies then synchronise the
+ *                 host).  They must stay valid until the stream has passed this
+ *                 call; Y_host is complete only after the stream is synchronised.
+ * X_dev, Y_dev    device staging buffers owned by the caller, with the
+ *                 alignment marlin_gemm requires; overwritten.
+ * Other arguments and errors as for marlin_gemm; a failed copy returns
+ * MARLIN_ERR_CUDA.  Argument errors are detected before anything is enqueued.
+ */
+marlin_status_t marlin_gemm_host(const uint16_t* X_host, uint16_t* X_dev, const void* packed,
+                                 const uint16_t* scales, const int32_t* zeros, uint16_t* Y_dev,
+                                 uint16_t* Y_host, int M, int K, int N, int group,
+                                 void* workspace, size_t workspace_bytes, marlin_stream_t stream);
+
+/*
  * Synchronises `stream`, reads and clears the device status word that
  * marlin_gemm keeps in `workspace`, and returns MARLIN_OK or
  * MARLIN_ERR_TIMEOUT (a bounded wait in a kernel expired; that call's Y is

@@ -165,3 +165,26 @@ def test_non_finite_propagates():
     y, _, _ = run_cuda(X, pack_codes(q), S, None, 128)
     assert np.isinf(y[0]).all() and (y[0] > 0).all()
     assert np.isnan(y[1]).all()
+
+
+@pytest.mark.parametrize("M,K,N,g,asym", [(4, 1024, 512, 128, False), (40, 2048, 384, 128, True)])
+def test_host_buffer_entry_point_matches_device_call(M, K, N, g, asym):
+    """marlin_gemm_host (copy in, multiply, copy out on one stream) returns the
+    same bits as marlin_gemm on device buffers; pinned and pageable host X."""
+    import w4a16_mixed_precision_gb300 as w4
+    from gpu_util import device
+    p = Problem("host", M, K, N, g, asym)
+    inp = make_inputs(p)
+    y_dev_ref, pw, ws = run_cuda(inp.X, inp.Qp, inp.S, inp.Zp, g)
+    dev = device()
+    for pin in (True, False):
+        xh = torch.from_numpy(inp.X.copy())
+        yh = torch.full((M, N), 7.0, dtype=torch.float16)
+        if pin:
+            xh, yh = xh.pin_memory(), yh.pin_memory()
+        xd = torch.empty((M, K), dtype=torch.float16, device=dev)
+        yd = torch.empty((M, N), dtype=torch.float16, device=dev)
+        w4.gemm_host(xh, xd, pw, ws, yd, yh)
+        torch.cuda.synchronize()
+        assert w4.device_status(ws) == 0
+        assert np.array_equal(yh.numpy().view(np.uint16), y_dev_ref.view(np.uint16))

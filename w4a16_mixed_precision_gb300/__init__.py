@@ -20,7 +20,7 @@ import torch
 from . import _binding
 from ._binding import MarlinError, status_string  # noqa: F401
 
-__all__ = ["PackedWeights", "Workspace", "repack", "gemm", "gemm_into", "device_status",
+__all__ = ["PackedWeights", "Workspace", "repack", "gemm", "gemm_into", "gemm_host", "device_status",
            "MarlinError", "status_string", "packed_layout"]
 
 
@@ -119,6 +119,29 @@ def gemm_into(x: torch.Tensor, w: PackedWeights, ws: Workspace, y: torch.Tensor)
 def gemm(x: torch.Tensor, w: PackedWeights, ws: Workspace) -> torch.Tensor:
     y = torch.empty((x.shape[0], w.N), dtype=torch.float16, device=x.device)
     return gemm_into(x, w, ws, y)
+
+
+def gemm_host(x_host: torch.Tensor, x_dev: torch.Tensor, w: PackedWeights, ws: Workspace,
+              y_dev: torch.Tensor, y_host: torch.Tensor) -> torch.Tensor:
+    """y_host[M, N] = x_host[M, K] . dequant(W) through device staging buffers,
+    all on the current stream (one library call: copy in, multiply, copy out).
+    Host tensors should be pinned; y_host is complete once the stream is
+    synchronised."""
+    for t, n in ((x_host, "x_host"), (y_host, "y_host")):
+        if t.device.type != "cpu" or t.dtype != torch.float16 or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous fp16 host tensor")
+    _need_cuda(x_dev, "x_dev", torch.float16)
+    _need_cuda(y_dev, "y_dev", torch.float16)
+    M, K = x_host.shape
+    if (K != w.K or tuple(x_dev.shape) != (M, K) or tuple(y_dev.shape) != (M, w.N)
+            or tuple(y_host.shape) != (M, w.N)):
+        raise ValueError("shape mismatch")
+    rc = _binding.gemm_host_raw(x_host.data_ptr(), x_dev.data_ptr(), w.codes_ptr, w.scales_ptr,
+                                w.zeros_ptr, y_dev.data_ptr(), y_host.data_ptr(), M, K, w.N, w.group,
+                                ws.ptr, ws.nbytes, _stream())
+    if rc != _binding.OK:
+        raise MarlinError(rc, "marlin_gemm_host")
+    return y_host
 
 
 def device_status(ws: Workspace) -> int:

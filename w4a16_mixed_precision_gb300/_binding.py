@@ -30,6 +30,7 @@ EXPORTS = (
     "marlin_workspace_bytes",
     "marlin_gemm",
     "marlin_gemm_no_alloc",
+    "marlin_gemm_host",
     "marlin_last_device_status",
 )
 
@@ -66,6 +67,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.marlin_last_device_status.argtypes = [P, P]
         lib.marlin_gemm_no_alloc.argtypes = [P, P, P, P, P, I, I, I, I, P]
         lib.marlin_gemm_no_alloc.restype = I
+        lib.marlin_gemm_host.argtypes = [P, P, P, P, P, P, P, I, I, I, I, P, SZ, P]
+        lib.marlin_gemm_host.restype = I
         for f in ("marlin_packed_layout", "marlin_repack", "marlin_workspace_bytes", "marlin_gemm",
                   "marlin_last_device_status"):
             getattr(lib, f).restype = I
@@ -109,6 +112,14 @@ def gemm_raw(x_ptr: int, packed_ptr: int, scales_ptr: int, zeros_ptr: int | None
     """Raw call; returns the status code."""
     return load().marlin_gemm(x_ptr, packed_ptr, scales_ptr, zeros_ptr or None, y_ptr, M, K, N,
                               group, ws_ptr, ws_bytes, stream or None)
+
+
+def gemm_host_raw(xh_ptr: int, xd_ptr: int, packed_ptr: int, scales_ptr: int, zeros_ptr: int | None,
+                  yd_ptr: int, yh_ptr: int, M: int, K: int, N: int, group: int, ws_ptr: int,
+                  ws_bytes: int, stream: int) -> int:
+    """Raw call of the host-buffer entry point; returns the status code."""
+    return load().marlin_gemm_host(xh_ptr, xd_ptr, packed_ptr, scales_ptr, zeros_ptr or None, yd_ptr,
+                                   yh_ptr, M, K, N, group, ws_ptr, ws_bytes, stream or None)
 
 
 def gemm_no_alloc_raw(x_ptr: int, packed_ptr: int, scales_ptr: int, zeros_ptr: int | None, y_ptr: int,

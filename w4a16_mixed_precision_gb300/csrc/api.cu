@@ -81,6 +81,23 @@ int small_m_max() {
   return v;
 }
 
+// Recently encoded tensor maps of X, per host thread (direct-mapped).
+struct XMapEntry {
+  CUtensorMap map;
+  const void* X;
+  int M, K, bn;
+  bool valid;
+};
+constexpr int kXMapSlots = 64;
+thread_local XMapEntry t_xmaps[kXMapSlots];
+
+int xmap_slot(const void* X, int M, int K, int bn) {
+  uint64_t h = (uint64_t)reinterpret_cast<uintptr_t>(X) >> 8;
+  h ^= (uint64_t)M * 0x9E3779B97F4A7C15ull ^ (uint64_t)K * 0xC2B2AE3D27D4EB4Full ^ (uint64_t)bn;
+  h ^= h >> 29;
+  return (int)(h & (kXMapSlots - 1));
+}
+
 // The partition plan.  A unit is one (m-tile, 128-column tile, K slice of
 // cpu*64 rows); the grid is one CTA per SM (fewer if there are fewer units),
 // each taking an equal contiguous stripe of units.
@@ -251,15 +268,26 @@ marlin_status_t marlin_gemm(const uint16_t* X, const void* packed, const uint16_
     }
   }
 
-  CUtensorMap x_map;
-  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kChunkK, (cuuint32_t)g.bn};
-  const cuuint32_t estr[2] = {1, 1};
-  if (g_encode(&x_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(X), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return MARLIN_ERR_CUDA;
+  // X's tensor map depends only on (address, M, K, box rows): keep the last
+  // few per host thread, so a decode loop over fixed buffers encodes each once
+  XMapEntry& xe = t_xmaps[xmap_slot(X, M, K, g.bn)];
+  if (!(xe.valid && xe.X == X && xe.M == M && xe.K == K && xe.bn == g.bn)) {
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kChunkK, (cuuint32_t)g.bn};
+    const cuuint32_t estr[2] = {1, 1};
+    xe.valid = false;
+    if (g_encode(&xe.map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(X), dims, strides,
+                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MARLIN_ERR_CUDA;
+    xe.X = X;
+    xe.M = M;
+    xe.K = K;
+    xe.bn = g.bn;
+    xe.valid = true;
+  }
+  const CUtensorMap& x_map = xe.map;
 
   GemmParams p{};
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -306,6 +334,37 @@ marlin_status_t marlin_gemm(const uint16_t* X, const void* packed, const uint16_
   const cudaError_t e = g.kind == kKernelSmallM ? launch_small_m(x_map, p, g.grid, g.smem_bytes, st)
                                                 : launch_gemm(x_map, p, g.grid, g.smem_bytes, st);
   if (e != cudaSuccess) return MARLIN_ERR_CUDA;
+  return MARLIN_OK;
+}
+
+marlin_status_t marlin_gemm_host(const uint16_t* X_host, uint16_t* X_dev, const void* packed,
+                                 const uint16_t* scales, const int32_t* zeros, uint16_t* Y_dev,
+                                 uint16_t* Y_host, int M, int K, int N, int group,
+                                 void* workspace, size_t workspace_bytes, marlin_stream_t stream) {
+  if (M < 0 || !valid_shape(K, N) || !normalise_group(K, &group)) return MARLIN_ERR_INVALID_ARG;
+  if (M == 0) return MARLIN_OK;
+  if (!X_host || !Y_host || !X_dev || !Y_dev || !packed || !scales || !workspace)
+    return MARLIN_ERR_INVALID_ARG;
+  if (!aligned16(X_dev) || !aligned16(packed) || !aligned16(scales) || (zeros && !aligned16(zeros)) ||
+      !aligned16(workspace) || (reinterpret_cast<uintptr_t>(Y_dev) & 1u))
+    return MARLIN_ERR_MISALIGNED;
+  {
+    int dev;
+    DeviceState* d;
+    marlin_status_t s = current_device(&dev);
+    if (s != MARLIN_OK) return s;
+    if ((s = device_state(dev, &d)) != MARLIN_OK) return s;
+    const GemmPlan g = make_plan(M, K, N, group, d->sms, d->smem_optin, zeros != nullptr);
+    if (workspace_bytes < g.ws_bytes) return MARLIN_ERR_WORKSPACE_TOO_SMALL;
+  }
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(X_dev, X_host, (size_t)M * K * 2, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return MARLIN_ERR_CUDA;
+  const marlin_status_t s = marlin_gemm(X_dev, packed, scales, zeros, Y_dev, M, K, N, group, workspace,
+                                        workspace_bytes, stream);
+  if (s != MARLIN_OK) return s;
+  if (cudaMemcpyAsync(Y_host, Y_dev, (size_t)M * N * 2, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MARLIN_ERR_CUDA;
   return MARLIN_OK;
 }
 
