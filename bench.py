@@ -171,14 +171,27 @@ def dist_setup(n_gpus: int):
     return rank, world, local
 
 
+def _dist_device():
+    """Device of the tensors exchanged by the process group (CPU for gloo)."""
+    import torch.distributed as dist
+    return "cuda" if dist.get_backend() == "nccl" else "cpu"
+
+
 def dist_max(v: float, world: int) -> float:
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=_dist_device())
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_throughput(step_bytes: int, ms_local: float, steps: int, world: int):
+    """Whole-job throughput of `world` replicas that each ran `steps` steps of
+    `step_bytes`: the slowest rank's time decides.  Returns (ms per step, GB/s)."""
+    ms_per_step = dist_max(ms_local, world) / steps
+    return ms_per_step, step_bytes * world / (ms_per_step * 1e-3) / 1e9
 
 
 def dist_barrier(world: int):
@@ -387,13 +400,10 @@ def run_gpu(args, problems, rank, world, local):
     torch.cuda.synchronize()
     time.sleep(0.25)
     sampler.stop()
-    ms_total = ev0.elapsed_time(ev1)
-    ms_total = dist_max(ms_total, world)
-    ms_per_step = ms_total / args.steps
+    ms_per_step, value = aggregate_throughput(step_bytes, ev0.elapsed_time(ev1), args.steps, world)
     for lk in layers:
         assert w4.device_status(ws[lk]) == 0, "a kernel reported an expired wait"
 
-    value = step_bytes * world / (ms_per_step * 1e-3) / 1e9
     launches = len(problems)
     achieved = step_bytes / (ms_per_step * 1e-3) / 1e9
     clocks = sampler.summary(t_wall0 - 1.2, t_wall1)
