@@ -85,6 +85,9 @@ __device__ __forceinline__ long long stripe_owner(long long u, long long U, long
 // CTA publishes at most one partial tile (from its first segment, then goes on
 // without waiting) and reduces at most one (at its very end), and no CTA ever
 // waits for a CTA that is itself waiting: the wait graph has no cycles.
+// Contributors publish their partial words tagged (st_partial) and add one to
+// the tile's arrival counter; the reducer polls the words it needs and the
+// counter, both with bounded waits, and leaves words and counter zeroed.
 
 __device__ __forceinline__ long long tile_reducer(long long tile, long long KT, long long U,
                                                   long long G) {
@@ -97,9 +100,64 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
   return v;
 }
 
-__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void red_relaxed_gpu_add(int* p, int v) {
+  asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+
+// Partial tiles of split tiles are published element by element: a partial
+// value v is stored as bits(v) ^ kPartTag, so that a zero word means "not
+// written yet" (the workspace starts zeroed and the reducer re-zeroes what it
+// read).  No fp32 result has the bits of kPartTag (a signalling-NaN payload
+// that arithmetic never produces), so a written word is never zero, and the
+// reducer needs no ordering between a contributor's stores: each word it
+// polls is either absent or final.
+constexpr uint32_t kPartTag = 0x7F800001u;
+
+__device__ __forceinline__ void st_partial(float* p, float v) {
+  __stcg(reinterpret_cast<unsigned int*>(p), __float_as_uint(v) ^ kPartTag);
+}
+
+__device__ __forceinline__ uint32_t ld_partial_raw(const float* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float partial_value(uint32_t raw) { return __uint_as_float(raw ^ kPartTag); }
+
+// Bounded poll until the words base[q * stride + off[i]] (q < nq, i < NO) are
+// all written, into raw[q * NO + i]; returns false on timeout (recorded) or
+// when the CTA is aborting.
+template <int NQ, int NO>
+__device__ __forceinline__ bool poll_partials(const float* base, size_t stride, const uint32_t (&off)[NO],
+                                              int nq, uint32_t (&raw)[NQ * NO], const WaitCtx& c) {
+#pragma unroll
+  for (int i = 0; i < NQ * NO; ++i) raw[i] = 0u;
+  uint64_t t0 = 0;
+#pragma unroll 1
+  for (int attempt = 0;; ++attempt) {
+    bool done = true;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q)
+      if (q < nq) {
+#pragma unroll
+        for (int i = 0; i < NO; ++i) {
+          if (raw[q * NO + i] == 0u) raw[q * NO + i] = ld_partial_raw(base + q * stride + off[i]);
+          done = done && raw[q * NO + i] != 0u;
+        }
+      }
+    if (done) return true;
+    if (*reinterpret_cast<volatile int*>(c.abort)) return false;
+    if (attempt == 0) {
+      t0 = global_timer_ns();
+    } else if (global_timer_ns() - t0 > c.timeout_ns) {
+      raise_timeout(c);
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
+
 
 // Bounded spin until *counter reaches `expected` (acquire).  Returns false on
 // timeout (recorded in the status word) or when the CTA is aborting.

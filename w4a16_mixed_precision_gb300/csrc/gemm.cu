@@ -42,7 +42,6 @@ struct Ctrl {
   uint64_t dfull;
   uint64_t dempty;
   uint64_t drain[2];
-  uint64_t red_arrive;  // dequant warps -> leader: partial tile stored (contributor)
   uint64_t red_go;      // leader -> dequant warps: all partials published (reducer)
   uint32_t tmem_base;
   int abort;
@@ -103,7 +102,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(ctrl->dempty), kNumDqWarps);
     mbar_init(bar(ctrl->drain[0]), 1);
     mbar_init(bar(ctrl->drain[1]), 1);
-    mbar_init(bar(ctrl->red_arrive), kNumDqWarps);
     mbar_init(bar(ctrl->red_go), 1);
     ctrl->abort = 0;
     fence_mbarrier_init();
@@ -360,25 +358,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long c_first = tile_reducer(tile, KT, U, G);
       const long long c_last = stripe_owner((long long)tile * KT + KT - 1, U, G);
       const bool reducer = !whole && (long long)blockIdx.x == c_first;
-      if (reducer) {
-        // reducer (this is its last segment): wait until the other
-        // contributors have published their partial tiles
-        if (dq == 0) {
-          if (lane == 0) {
-            if (wait_counter(&p.counters[tile], (int)(c_last - c_first), wc))
-              p.counters[tile] = 0;  // leave the workspace zeroed for the next call
-            mbar_arrive(bar(ctrl->red_go));
-          }
-          __syncwarp();
+      if (reducer && dq == 0) {
+        // reducer (this is its last segment): the leader waits for the count
+        // of contributors, while every thread polls its own words of their
+        // partial tiles (a tagged word is final once non-zero)
+        if (lane == 0) {
+          if (wait_counter(&p.counters[tile], (int)(c_last - c_first), wc))
+            p.counters[tile] = 0;  // leave the workspace zeroed for the next call
+          mbar_arrive(bar(ctrl->red_go));
         }
-        if (!wait_warp(bar(ctrl->red_go), 0, wc)) break;
-        if (*reinterpret_cast<volatile int*>(&ctrl->abort)) break;
+        __syncwarp();
       }
       float* part = p.partials + (size_t)blockIdx.x * ((size_t)p.bn * kTileN);
+      const size_t part_stride = (size_t)p.bn * kTileN;
       // accumulators holding units of this tile: both, or the one of its only unit
       const bool alt = nacc == 2 && !p.split_n;
       const bool two = alt && seg_len >= 2;
       const uint32_t d_first = (alt && seg_len == 1) ? (uint32_t)(((u - u_begin) & 1) * p.bn) : 0u;
+      bool got = true, go_seen = !reducer;
       for (int cc = wg; cc < p.bn / 8; cc += kNumDqWG) {
         uint32_t r[8], r1[8];
         tmem_ld_x8(tmem + lane_off + d_first + (uint32_t)cc * 8, r);
@@ -390,24 +387,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc[c] = two ? __uint_as_float(r[c]) + __uint_as_float(r1[c]) : __uint_as_float(r[c]);
         if (reducer) {
           // own partial first, then the others' in stripe order (fixed order,
-          // bit-reproducible); loads of 2 contributors are issued together
+          // bit-reproducible); each word is re-zeroed once read
+          uint32_t off[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) off[c] = (uint32_t)((cc * 8 + c) * kTileN + row);
           for (long long q0 = c_first + 1; q0 <= c_last; q0 += 2) {
-            float v[2][8];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              if (q0 + j <= c_last) {
-                const float* qp = p.partials + (size_t)(q0 + j) * ((size_t)p.bn * kTileN) +
-                                  (size_t)(cc * 8) * kTileN + row;
-#pragma unroll
-                for (int c = 0; c < 8; ++c) v[j][c] = __ldcg(qp + (size_t)c * kTileN);
-              }
-            }
+            const int nq = (int)min(2LL, c_last - q0 + 1);
+            float* base = p.partials + (size_t)q0 * part_stride;
+            uint32_t raw[16];
+            if (!poll_partials<2, 8>(base, part_stride, off, nq, raw, wc)) { got = false; break; }
 #pragma unroll
             for (int j = 0; j < 2; ++j)
-              if (q0 + j <= c_last) {
+              if (j < nq) {
 #pragma unroll
-                for (int c = 0; c < 8; ++c) acc[c] += v[j][c];
+                for (int c = 0; c < 8; ++c) {
+                  acc[c] += partial_value(raw[j * 8 + c]);
+                  __stcg(base + j * part_stride + off[c], 0.f);
+                }
               }
+          }
+          if (!got) break;
+          if (!go_seen) {
+            if (!wait_warp(bar(ctrl->red_go), 0, wc) || *reinterpret_cast<volatile int*>(&ctrl->abort)) {
+              got = false;
+              break;
+            }
+            go_seen = true;
           }
         }
 #pragma unroll
@@ -417,27 +422,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (m_base + m < p.M)
               p.Y[(size_t)(m_base + m) * p.N + y_col] = __half_as_ushort(__float2half_rn(acc[c]));
           } else {
-            part[(size_t)m * kTileN + row] = acc[c];
+            st_partial(part + (size_t)m * kTileN + row, acc[c]);
           }
         }
       }
+      if (!got) break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(ctrl->dempty));
-
-      if (!whole && !reducer) {
-        // contributor (this is its first segment): publish the partial tile
-        // with one release increment and go on.
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(ctrl->red_arrive));
-        if (dq == 0) {
-          if (!wait_warp(bar(ctrl->red_arrive), 0, wc)) break;
-          // the release is cumulative: it also orders the other warps'
-          // stores, which this thread observed through the mbarrier
-          if (lane == 0) red_release_gpu_add(&p.counters[tile], 1);
-          __syncwarp();
-        }
-      }
+      // contributor (this is its first segment): its tagged words are its
+      // publication; count it in and go on without waiting
+      if (!whole && !reducer && dq == 0 && lane == 0) red_relaxed_gpu_add(&p.counters[tile], 1);
       ++seg;
       u += seg_len;
       ku = 0;

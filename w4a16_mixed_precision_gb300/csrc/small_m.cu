@@ -43,7 +43,6 @@ struct SmCtrl {
   uint64_t empty[kMaxStages];
   uint64_t red_full;    // odd-half warps -> even-half warps: accumulators in smem
   uint64_t red_free;    // even-half warps -> odd-half warps: exchange buffer read
-  uint64_t red_arrive;  // even-half warps -> leader: partial tile stored (contributor)
   uint64_t red_go;      // leader -> even-half warps: all partials published (reducer)
   int abort;
 };
@@ -90,7 +89,6 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     }
     mbar_init(bar(ctrl->red_full), kSmConsumers / 2);
     mbar_init(bar(ctrl->red_free), kSmConsumers / 2);
-    mbar_init(bar(ctrl->red_arrive), kSmConsumers / 2);
     mbar_init(bar(ctrl->red_go), 1);
     ctrl->abort = 0;
     fence_mbarrier_init();
@@ -276,28 +274,23 @@ __global__ void __launch_bounds__(kSmThreads, 1)
           const long long c_first = tile_reducer(tile, KT, U, G);
           const long long c_last = stripe_owner((long long)tile * KT + KT - 1, U, G);
           if ((long long)blockIdx.x != c_first) {
-            // contributor (this is its first segment): store the partial tile,
-            // publish it with one release increment, and go on
+            // contributor (this is its first segment): publish the partial tile
+            // word by word (tagged), count itself in, and go on without waiting
             float* part = p.partials + (size_t)blockIdx.x * ((size_t)p.bn * kTileN);
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
               for (int d = 0; d < 4; ++d) {
                 const int m = 8 * nb + ((d & 1) ? tok1 : tok0);
-                part[(size_t)m * kTileN + col_r + 8 * (d >> 1)] = acc[nb][d];
+                st_partial(part + (size_t)m * kTileN + col_r + 8 * (d >> 1), acc[nb][d]);
               }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(ctrl->red_arrive));
-            if (g == 0) {
-              if (!wait_warp(bar(ctrl->red_arrive), 0, wc)) break;
-              // the release is cumulative: it also orders the other warps'
-              // stores, which this thread observed through the mbarrier
-              if (lane == 0) red_release_gpu_add(&p.counters[tile], 1);
-              __syncwarp();
-            }
+            if (g == 0 && lane == 0) red_relaxed_gpu_add(&p.counters[tile], 1);
           } else {
-            // reducer (this is its last segment): wait for the other
-            // contributors, then sum in stripe order -- own partial first
+            // reducer (this is its last segment): every thread polls its own
+            // words of the other contributors' partials (a word is final once
+            // non-zero) and sums in stripe order, own partial first; the leader
+            // also waits for the arrival count, which must reach the number of
+            // contributors before Y is written
             if (g == 0) {
               if (lane == 0) {
                 if (wait_counter(&p.counters[tile], (int)(c_last - c_first), wc))
@@ -306,38 +299,42 @@ __global__ void __launch_bounds__(kSmThreads, 1)
               }
               __syncwarp();
             }
-            if (!wait_warp(bar(ctrl->red_go), 0, wc)) break;
-            if (*reinterpret_cast<volatile int*>(&ctrl->abort)) break;
+            bool got = true;
 #pragma unroll
-            for (int nb = 0; nb < NB; ++nb) {
-              float tot[4] = {acc[nb][0], acc[nb][1], acc[nb][2], acc[nb][3]};
-              for (long long q0 = c_first + 1; q0 <= c_last; q0 += 8) {
-                float v[8][4];
+            for (int nb = 0; nb < NB && got; ++nb) {
+              // the sums build up in acc (own partial first)
+              uint32_t off[4];
 #pragma unroll
-                for (int jq = 0; jq < 8; ++jq) {
-                  if (q0 + jq <= c_last) {
-                    const float* qp = p.partials + (size_t)(q0 + jq) * ((size_t)p.bn * kTileN);
+              for (int d = 0; d < 4; ++d)
+                off[d] = (uint32_t)((8 * nb + ((d & 1) ? tok1 : tok0)) * kTileN + col_r + 8 * (d >> 1));
+              const size_t stride = (size_t)p.bn * kTileN;
+              for (long long q0 = c_first + 1; q0 <= c_last && got; q0 += 4) {
+                const int nq = (int)min(4LL, c_last - q0 + 1);
+                float* base = p.partials + (size_t)q0 * stride;
+                uint32_t raw[16];
+                if (!poll_partials<4, 4>(base, stride, off, nq, raw, wc)) { got = false; break; }
 #pragma unroll
-                    for (int d = 0; d < 4; ++d)
-                      v[jq][d] = __ldcg(qp + (size_t)(8 * nb + ((d & 1) ? tok1 : tok0)) * kTileN +
-                                        col_r + 8 * (d >> 1));
-                  }
-                }
+                for (int jq = 0; jq < 4; ++jq)
+                  if (jq < nq) {
 #pragma unroll
-                for (int jq = 0; jq < 8; ++jq)
-                  if (q0 + jq <= c_last) {
-#pragma unroll
-                    for (int d = 0; d < 4; ++d) tot[d] += v[jq][d];
+                    for (int d = 0; d < 4; ++d) {
+                      acc[nb][d] += partial_value(raw[jq * 4 + d]);
+                      __stcg(base + jq * stride + off[d], 0.f);  // re-zero for the next call
+                    }
                   }
               }
+            }
+            if (!wait_warp(bar(ctrl->red_go), 0, wc)) break;
+            if (!got || *reinterpret_cast<volatile int*>(&ctrl->abort)) break;
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
               for (int d = 0; d < 4; ++d) {
                 const int m = 8 * nb + ((d & 1) ? tok1 : tok0);
                 if (m < p.M)
                   p.Y[(size_t)m * p.N + y_col0 + 8 * (d >> 1)] =
-                      __half_as_ushort(__float2half_rn(tot[d]));
+                      __half_as_ushort(__float2half_rn(acc[nb][d]));
               }
-            }
           }
         }
       }
