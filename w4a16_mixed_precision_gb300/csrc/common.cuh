@@ -177,31 +177,6 @@ static __device__ __noinline__ bool wait_counter(const int* counter, int expecte
 
 // ---- dequantisation -------------------------------------------------------------
 
-__device__ __forceinline__ __half2 as_h2(uint32_t v) {
-  return *reinterpret_cast<__half2*>(&v);
-}
-__device__ __forceinline__ uint32_t as_u32(__half2 v) {
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// fp16x2 arithmetic on raw 32-bit registers, round to nearest even (explicit
-// rounding also keeps the compiler from fusing a multiply into an add).
-__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-__device__ __forceinline__ uint32_t f16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-
 // One 32-bit word of 8 codes -> the four fp16 pairs of a 16x16 operand
 // fragment: h[0] = column r, rows k..k+1; h[1] = column r+8, rows k..k+1;
 // h[2] = column r, rows k+2..k+3; h[3] = column r+8, rows k+2..k+3 (the
@@ -209,38 +184,25 @@ __device__ __forceinline__ uint32_t f16x2_fma(uint32_t a, uint32_t b, uint32_t c
 // ulp is 1 on [1024, 2048)); 0x6400 | (c << 4) is 1024 + 16c.  Subtracting
 // 1024 + z (or scaling by 1/16 and adding -(64 + z)) gives q - z exactly; the
 // single rounding of the dequantisation is the final multiply by the scale.
-// Arguments are fp16 pairs in 32-bit registers.
-__device__ __forceinline__ void dequant_frag(uint32_t w, uint32_t sub_r, uint32_t add_r8, uint32_t s_r,
-                                             uint32_t s_r8, uint32_t (&h)[4]) {
-  const uint32_t sixteenth = 0x2C002C00u;
-  const uint32_t w8 = w >> 8;
-  const uint32_t a = (w & 0x000F000Fu) | 0x64006400u;
-  const uint32_t b = (w & 0x00F000F0u) | 0x64006400u;
-  const uint32_t c = (w8 & 0x000F000Fu) | 0x64006400u;
-  const uint32_t d = (w8 & 0x00F000F0u) | 0x64006400u;
-  h[0] = f16x2_mul(f16x2_sub(a, sub_r), s_r);
-  h[1] = f16x2_mul(f16x2_fma(b, sixteenth, add_r8), s_r8);
-  h[2] = f16x2_mul(f16x2_sub(c, sub_r), s_r);
-  h[3] = f16x2_mul(f16x2_fma(d, sixteenth, add_r8), s_r8);
-}
+// Arguments are fp16 pairs in 32-bit registers.  The blocks of PTX below
+// implement this for one word and feed the result straight to its consumer.
 
-// The same dequantisation fused with the tensor-core multiply-accumulates that
+// This dequantisation fused with the tensor-core multiply-accumulates that
 // consume it, as one block of PTX: the four fp16 pairs are produced directly in
 // the registers the mma.sync A operand reads (written as separate statements,
 // the compiler surrounds them with register moves).  NB mma.sync.m16n8k16 share
 // the A fragment, one per block of 8 tokens: acc[nb] += A * B[nb].
-#define W4A16_DEQ_PTX(W, SUB, ADD, S, S8)                                 \
-  ".reg .b32 t0, t1, t2, t3, w8, k16;\n\t"                                \
-  "mov.b32 k16, 0x2C002C00;\n\t"                                         \
+#define W4A16_DEQ_PTX(W, SUB, ADD, S, S8, K16)                            \
+  ".reg .b32 t0, t1, t2, t3, w8;\n\t"                                     \
   "lop3.b32 t0, " W ", 0x000F000F, 0x64006400, 0xEA;\n\t"                \
   "lop3.b32 t1, " W ", 0x00F000F0, 0x64006400, 0xEA;\n\t"                \
   "shr.u32 w8, " W ", 8;\n\t"                                             \
   "lop3.b32 t2, w8, 0x000F000F, 0x64006400, 0xEA;\n\t"                    \
   "lop3.b32 t3, w8, 0x00F000F0, 0x64006400, 0xEA;\n\t"                    \
   "sub.rn.f16x2 t0, t0, " SUB ";\n\t"                                     \
-  "fma.rn.f16x2 t1, t1, k16, " ADD ";\n\t"                                \
+  "fma.rn.f16x2 t1, t1, " K16 ", " ADD ";\n\t"                           \
   "sub.rn.f16x2 t2, t2, " SUB ";\n\t"                                     \
-  "fma.rn.f16x2 t3, t3, k16, " ADD ";\n\t"                                \
+  "fma.rn.f16x2 t3, t3, " K16 ", " ADD ";\n\t"                           \
   "mul.rn.f16x2 t0, t0, " S ";\n\t"                                       \
   "mul.rn.f16x2 t1, t1, " S8 ";\n\t"                                      \
   "mul.rn.f16x2 t2, t2, " S ";\n\t"                                       \
@@ -253,21 +215,22 @@ template <int NB>
 __device__ __forceinline__ void dequant_mma(float (&acc)[NB][4], uint32_t w, uint32_t sub_r,
                                             uint32_t add_r8, uint32_t s_r, uint32_t s_r8,
                                             const uint2 (&b)[NB]) {
+  const uint32_t k16 = 0x2C002C00u;  // 1/16 as an fp16 pair (an operand, so it is materialised once)
   if constexpr (NB == 1) {
-    asm volatile("{\n\t" W4A16_DEQ_PTX("%4", "%5", "%6", "%7", "%8")
+    asm volatile("{\n\t" W4A16_DEQ_PTX("%4", "%5", "%6", "%7", "%8", "%11")
                  W4A16_MMA_PTX("%0", "%1", "%2", "%3", "%9", "%10") "}"
                  : "+f"(acc[0][0]), "+f"(acc[0][1]), "+f"(acc[0][2]), "+f"(acc[0][3])
-                 : "r"(w), "r"(sub_r), "r"(add_r8), "r"(s_r), "r"(s_r8), "r"(b[0].x), "r"(b[0].y));
+                 : "r"(w), "r"(sub_r), "r"(add_r8), "r"(s_r), "r"(s_r8), "r"(b[0].x), "r"(b[0].y), "r"(k16));
   } else if constexpr (NB == 2) {
-    asm volatile("{\n\t" W4A16_DEQ_PTX("%8", "%9", "%10", "%11", "%12")
+    asm volatile("{\n\t" W4A16_DEQ_PTX("%8", "%9", "%10", "%11", "%12", "%17")
                  W4A16_MMA_PTX("%0", "%1", "%2", "%3", "%13", "%14")
                  W4A16_MMA_PTX("%4", "%5", "%6", "%7", "%15", "%16") "}"
                  : "+f"(acc[0][0]), "+f"(acc[0][1]), "+f"(acc[0][2]), "+f"(acc[0][3]),
                    "+f"(acc[1][0]), "+f"(acc[1][1]), "+f"(acc[1][2]), "+f"(acc[1][3])
                  : "r"(w), "r"(sub_r), "r"(add_r8), "r"(s_r), "r"(s_r8), "r"(b[0].x), "r"(b[0].y),
-                   "r"(b[1].x), "r"(b[1].y));
+                   "r"(b[1].x), "r"(b[1].y), "r"(k16));
   } else if constexpr (NB == 3) {
-    asm volatile("{\n\t" W4A16_DEQ_PTX("%12", "%13", "%14", "%15", "%16")
+    asm volatile("{\n\t" W4A16_DEQ_PTX("%12", "%13", "%14", "%15", "%16", "%23")
                  W4A16_MMA_PTX("%0", "%1", "%2", "%3", "%17", "%18")
                  W4A16_MMA_PTX("%4", "%5", "%6", "%7", "%19", "%20")
                  W4A16_MMA_PTX("%8", "%9", "%10", "%11", "%21", "%22") "}"
@@ -275,10 +238,10 @@ __device__ __forceinline__ void dequant_mma(float (&acc)[NB][4], uint32_t w, uin
                    "+f"(acc[1][0]), "+f"(acc[1][1]), "+f"(acc[1][2]), "+f"(acc[1][3]),
                    "+f"(acc[2][0]), "+f"(acc[2][1]), "+f"(acc[2][2]), "+f"(acc[2][3])
                  : "r"(w), "r"(sub_r), "r"(add_r8), "r"(s_r), "r"(s_r8), "r"(b[0].x), "r"(b[0].y),
-                   "r"(b[1].x), "r"(b[1].y), "r"(b[2].x), "r"(b[2].y));
+                   "r"(b[1].x), "r"(b[1].y), "r"(b[2].x), "r"(b[2].y), "r"(k16));
   } else {
     static_assert(NB == 4, "NB must be 1..4");
-    asm volatile("{\n\t" W4A16_DEQ_PTX("%16", "%17", "%18", "%19", "%20")
+    asm volatile("{\n\t" W4A16_DEQ_PTX("%16", "%17", "%18", "%19", "%20", "%29")
                  W4A16_MMA_PTX("%0", "%1", "%2", "%3", "%21", "%22")
                  W4A16_MMA_PTX("%4", "%5", "%6", "%7", "%23", "%24")
                  W4A16_MMA_PTX("%8", "%9", "%10", "%11", "%25", "%26")
@@ -288,7 +251,7 @@ __device__ __forceinline__ void dequant_mma(float (&acc)[NB][4], uint32_t w, uin
                    "+f"(acc[2][0]), "+f"(acc[2][1]), "+f"(acc[2][2]), "+f"(acc[2][3]),
                    "+f"(acc[3][0]), "+f"(acc[3][1]), "+f"(acc[3][2]), "+f"(acc[3][3])
                  : "r"(w), "r"(sub_r), "r"(add_r8), "r"(s_r), "r"(s_r8), "r"(b[0].x), "r"(b[0].y),
-                   "r"(b[1].x), "r"(b[1].y), "r"(b[2].x), "r"(b[2].y), "r"(b[3].x), "r"(b[3].y));
+                   "r"(b[1].x), "r"(b[1].y), "r"(b[2].x), "r"(b[2].y), "r"(b[3].x), "r"(b[3].y), "r"(k16));
   }
 }
 
