@@ -117,9 +117,13 @@ __device__ __forceinline__ void st_partial(float* p, float v) {
   __stcg(reinterpret_cast<unsigned int*>(p), __float_as_uint(v) ^ kPartTag);
 }
 
+// An L2 load (not cached in L1) of one tagged word.  Each word is written
+// once per call and validates itself, so a plain cache-global load suffices;
+// measured, strong (relaxed.gpu) loads of a batch of words took several times
+// longer to come back.
 __device__ __forceinline__ uint32_t ld_partial_raw(const float* p) {
   uint32_t v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
@@ -136,15 +140,21 @@ __device__ __forceinline__ bool poll_partials(const float* base, size_t stride, 
   uint64_t t0 = 0;
 #pragma unroll 1
   for (int attempt = 0;; ++attempt) {
+    // issue every missing word's load first, then test them all: the loads
+    // are in flight together (one round trip per attempt)
+#pragma unroll
+    for (int q = 0; q < NQ; ++q)
+      if (q < nq) {
+#pragma unroll
+        for (int i = 0; i < NO; ++i)
+          if (raw[q * NO + i] == 0u) raw[q * NO + i] = ld_partial_raw(base + q * stride + off[i]);
+      }
     bool done = true;
 #pragma unroll
     for (int q = 0; q < NQ; ++q)
       if (q < nq) {
 #pragma unroll
-        for (int i = 0; i < NO; ++i) {
-          if (raw[q * NO + i] == 0u) raw[q * NO + i] = ld_partial_raw(base + q * stride + off[i]);
-          done = done && raw[q * NO + i] != 0u;
-        }
+        for (int i = 0; i < NO; ++i) done = done && raw[q * NO + i] != 0u;
       }
     if (done) return true;
     if (*reinterpret_cast<volatile int*>(c.abort)) return false;
