@@ -439,10 +439,15 @@ def run_gpu(args, problems, rank, world, local):
         "runs": runs,
     }
     if args.workload == "prefill":
+        # the timed region replays the step for seconds under the power cap:
+        # the sustained (seconds-long) dense rate is the denominator
         tf = step_flops / (ms_per_step * 1e-3) / 1e12
-        line["roofline"] = {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
-                            "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"], "traffic": None,
-                            "peak_source": peaks["source"] + " bf16 (fp16 dense rate is the same)",
+        pk = peaks["bf16_tflops_sustained"]
+        line["roofline"] = {"bound": "tensor", "achieved": tf, "peak": pk,
+                            "unit": "TFLOP/s", "frac": tf / pk, "traffic": None,
+                            "peak_source": peaks["source"] + " bf16 sustained (fp16 dense rate is the same); "
+                                           f"burst {peaks['bf16_tflops']:.0f} TFLOP/s -> "
+                                           f"{tf / peaks['bf16_tflops']:.3f}",
                             "kernel": kernel_names(problems)}
     if rank == 0 and not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
