@@ -315,8 +315,6 @@ marlin_status_t marlin_gemm(const uint16_t* X, const void* packed, const uint16_
   p.off_codes = (uint32_t)g.cpu * p.x_chunk_bytes;
   p.off_scales = p.off_codes + (uint32_t)g.cpu * kChunkCodeBytes;
   p.off_zeros = p.off_scales + (uint32_t)g.n_g * kTileN * 2;
-  p.tx_bytes = (uint32_t)g.cpu * (p.x_chunk_bytes + kChunkCodeBytes) + kTileN * 2 +
-               (zeros ? kTileN / 2 : 0);
   p.weights_reused = g.m_tiles > 1;
   p.nacc = g.nacc > 0 ? g.nacc : 1;
   p.split_n = g.split_n;

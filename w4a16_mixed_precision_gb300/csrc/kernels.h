@@ -40,7 +40,6 @@ struct GemmParams {
   uint32_t stage_bytes;
   uint32_t x_chunk_bytes;   // bn * 128
   uint32_t off_codes, off_scales, off_zeros;  // byte offsets inside a stage
-  uint32_t tx_bytes;        // bytes landed per stage
   int weights_reused;       // more than one m-tile reads the same weights
   int nacc;                 // tcgen05 kernel: MMA issuers, each with its own accumulator (1 or 2)
   int split_h;              // split_n: token columns of the first issuer (multiple of 16)
