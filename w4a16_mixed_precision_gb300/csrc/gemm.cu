@@ -19,10 +19,12 @@
 //     pipeline"); warps 4..19 (four warpgroups, taking whole units in turn)
 //     turn 4-bit codes into fp16 with the 0x6400 exponent trick, scale them
 //     with one fp16 multiply, and store the result straight into tensor memory
-//     as the A operand; warps 1 and 2 issue tcgen05.mma for alternate units of
-//     a tile (A from TMEM, B = X from shared memory, fp32 accumulators in
-//     TMEM, one each); the dequant warps then read the accumulators back with
-//     tcgen05.ld and write fp16 Y (or fp32 partials).
+//     as the A operand; warps 1 and 2 issue tcgen05.mma (A from TMEM, B = X
+//     from shared memory, fp32 accumulators in TMEM): for bn <= 128 on
+//     alternate units, one accumulator each, and for bn > 128 on every unit,
+//     splitting the token columns of one accumulator at 128; the dequant warps
+//     then read the accumulators back with tcgen05.ld and write fp16 Y (or
+//     tagged fp32 partial words).
 //   * Every wait is bounded (global timer); on expiry the kernel records
 //     kStatusTimeout in the status word, drains its own copies and MMAs, frees
 //     TMEM and returns.
