@@ -120,20 +120,10 @@ __device__ __forceinline__ void tc_fence_after() {
 
 // ---- tcgen05: MMA ---------------------------------------------------------------
 
-// D[tmem] (+)= A[tmem] * B[smem desc]; kind::f16 (fp16 inputs, fp32 accumulate).
-__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                           uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// The same MMA issued from warp-uniform code: every lane executes the call and
-// the lane picked by elect.sync (the lowest active one) issues it, so the
-// operands can stay in uniform registers.
+// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16 (fp16 inputs, fp32 accumulate;
+// accumulate = 0 overwrites D), issued from warp-uniform code: every lane
+// executes the call and the lane picked by elect.sync (the lowest active one)
+// issues it, so the operands can stay in uniform registers.
 __device__ __forceinline__ void mma_f16_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                  uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -145,8 +135,9 @@ __device__ __forceinline__ void mma_f16_ts_elect(uint32_t d_tmem, uint32_t a_tme
       : "memory");
 }
 
-// tcgen05.commit from warp-uniform code, by the lane elect.sync picks (the
-// one that issued the MMAs above).
+// tcgen05.commit from warp-uniform code, by the lane elect.sync picks (the one
+// that issued the MMAs above): arrives once on `bar` when every tcgen05.mma
+// that lane issued so far has completed.
 __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\t"
@@ -155,27 +146,7 @@ __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
       : "memory");
 }
 
-// Arrive once on `bar` when every tcgen05.mma this thread issued so far completes.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-// ---- tcgen05: TMEM <-> registers (32 lanes x 32-bit shape) -----------------------
-
-__device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
-      "%29, %30, %31, %32};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
-      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
-      "r"(v[29]), "r"(v[30]), "r"(v[31])
-      : "memory");
-}
+// ---- tcgen05: TMEM <-> registers ----------------------------------------------------
 
 // 16 lanes x 256 bits, 4 repetitions along the columns (32 columns).  For each
 // repetition r, thread t holds (lane base + t/4, column 8r + 2(t%4)),
