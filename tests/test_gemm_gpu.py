@@ -188,3 +188,37 @@ def test_host_buffer_entry_point_matches_device_call(M, K, N, g, asym):
         torch.cuda.synchronize()
         assert w4.device_status(ws) == 0
         assert np.array_equal(yh.numpy().view(np.uint16), y_dev_ref.view(np.uint16))
+
+
+def test_linear_layer_from_gptq_and_awq_weights():
+    """W4A16Linear (repack at construction, one marlin_gemm per forward) on
+    GPTQ-order and AWQ-order copies of the same weights, against the oracle;
+    leading batch dimensions are flattened into M."""
+    from w4a16_mixed_precision_gb300.formats import AWQ_ORDER
+    from w4a16_mixed_precision_gb300.layer import W4A16Linear
+    p = Problem("layer", 6, 1024, 384, 128, True)
+    inp = make_inputs(p)
+    ref = oracle.w4a16(inp.X, inp.Qp, inp.S, inp.Zp, p.group, p.N)
+    dev = torch.device("cuda", 0)
+    x = torch.from_numpy(inp.X).to(dev).reshape(2, 3, p.K)
+    lin = W4A16Linear(torch.from_numpy(inp.Qp), torch.from_numpy(inp.S), torch.from_numpy(inp.Zp), p.group)
+    y = lin(x)
+    assert tuple(y.shape) == (2, 3, p.N)
+    ok, err, _ = oracle.within_tolerance(y.reshape(p.M, p.N).cpu().numpy(), ref)
+    assert ok, f"GPTQ-order layer: max abs err {err}"
+    # the same weights in AWQ order (columns packed, interleaved)
+    q = oracle.unpack_codes(inp.Qp, p.K, p.N)
+    z = oracle.unpack_zeros(inp.Zp, p.G, p.N)
+
+    def awq_pack(codes):
+        R, C = codes.shape
+        out = np.zeros((R, C // 8), np.uint64)
+        for c in range(C // 8):
+            for i, col in enumerate(AWQ_ORDER):
+                out[:, c] |= codes[:, 8 * c + col].astype(np.uint64) << np.uint64(4 * i)
+        return out.astype(np.uint32).view(np.int32)
+
+    lin2 = W4A16Linear.from_awq(awq_pack(np.asarray(q, np.uint32)), torch.from_numpy(inp.S),
+                                awq_pack(np.asarray(z, np.uint32)), p.group)
+    y2 = lin2(x)
+    assert np.array_equal(y2.cpu().numpy().view(np.uint16), y.cpu().numpy().view(np.uint16))

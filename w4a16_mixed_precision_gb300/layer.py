@@ -1,0 +1,61 @@
+"""A linear layer over the fused W4A16 kernel: y = x . dequant(W).
+
+The pages describe the kernel as used through a torch module that converts and
+holds the compressed weights ("Marlin Project Overview", section "Requirements
+and Usage": a torch module converts and holds the compressed data; users with
+suitably prepared weights and scales may also call the kernel directly) and repack at load time ("Marlin /
+GPTQ-Marlin", section "Tiled layout et repacking").  Here construction repacks
+once on the GPU and every forward call is one marlin_gemm launch; there is no
+bias and no other arithmetic outside the kernel.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import Workspace, gemm_into, repack
+from .formats import awq_to_gptq
+
+
+class W4A16Linear(torch.nn.Module):
+    """y[..., N] = x[..., K] . dequant(W)[K, N], fp16 in and out, fp32 accumulation."""
+
+    def __init__(self, qweight: torch.Tensor, scales: torch.Tensor, qzeros: torch.Tensor | None = None,
+                 group: int = 128, device=None):
+        """qweight: GPTQ-order int32 [K/8, N]; scales fp16 [K/group, N]; qzeros
+        int32 [K/group, N/8] or None (z = 8); group 128, a multiple of 128
+        dividing K, or -1/K for one scale per column."""
+        super().__init__()
+        dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        q = qweight.to(dev, torch.int32).contiguous()
+        s = scales.to(dev, torch.float16).contiguous()
+        z = None if qzeros is None else qzeros.to(dev, torch.int32).contiguous()
+        self.K, self.N = q.shape[0] * 8, q.shape[1]
+        self.group = self.K if group == -1 else group
+        self.packed = repack(q, s, z, self.group)
+        self._ws = None
+        self._ws_m = 0
+
+    @classmethod
+    def from_awq(cls, qweight: np.ndarray, scales, qzeros: np.ndarray | None = None, group: int = 128,
+                 device=None) -> "W4A16Linear":
+        """From AWQ-order int32 codes [K, N/8] (and zeros [K/group, N/8])."""
+        codes, zeros = awq_to_gptq(np.asarray(qweight), None if qzeros is None else np.asarray(qzeros))
+        return cls(torch.from_numpy(codes), torch.as_tensor(scales),
+                   None if zeros is None else torch.from_numpy(zeros), group, device)
+
+    def _workspace(self, M: int) -> Workspace:
+        if self._ws is None or M > self._ws_m:
+            self._ws = Workspace(M, self.K, self.N, self.group, device=self.packed.buf.device)
+            self._ws_m = M
+        return self._ws
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        if x.shape[-1] != self.K:
+            raise ValueError(f"expected last dimension {self.K}, got {x.shape[-1]}")
+        lead = x.shape[:-1]
+        x2 = x.reshape(-1, self.K).contiguous()
+        y = torch.empty((x2.shape[0], self.N), dtype=torch.float16, device=x2.device)
+        if x2.shape[0] > 0:
+            gemm_into(x2, self.packed, self._workspace(x2.shape[0]), y)
+        return y.reshape(*lead, self.N)
