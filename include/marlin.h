@@ -119,7 +119,8 @@ marlin_status_t marlin_workspace_bytes(int M, int K, int N, int group, int devic
  * zeros      device, the zeros region (packed + off_zeros), or NULL for z = 8.
  * Y          device, fp16 [M][N] row-major, written; must not overlap inputs.
  * workspace  device, >= marlin_workspace_bytes(...) bytes, 16-byte aligned.
- *            Zero it once after allocating; every call leaves it zeroed again.
+ *            Zero it once after allocating; every call leaves it zeroed again
+ *            (after a call that reports MARLIN_ERR_TIMEOUT, zero it again).
  *            Calls that share a workspace must be ordered (same stream, or
  *            events): concurrent calls on one workspace race.
  * Result is deterministic: the same inputs give bit-identical Y on every run.
@@ -150,8 +151,8 @@ marlin_status_t marlin_gemm(const uint16_t* X, const void* packed, const uint16_
  * launched; other argument errors as for marlin_gemm.
  * Set-up: the first call on a device looks up the array's device address
  * (once per device, with that device current); make that first call before
- * any stream capture.  Each call clears the status word and tile counters on
- * `stream` before launching.
+ * any stream capture.  Each call clears the part of the array it uses (status
+ * word, tile counters, partial tiles) on `stream` before launching.
  * All calls share one array: calls that overlap on the GPU (different
  * streams, or different host threads on one device without ordering) race and
  * give wrong results.  A bounded wait that expires inside the kernel is

@@ -40,6 +40,9 @@ SMALL_CASES = [
     (33, 1024, 640, 1024, True),       # one scale per column, ragged M
     (48, 2048, 768, 128, True),
     (64, 1536, 512, 512, False),       # group 512
+    (12, 2048, 640, 256, True),        # group 256, warp-level kernel
+    (80, 2048, 384, 256, False),       # group 256, tcgen05 kernel
+    (300, 1024, 256, 1024, True),      # one scale per column, two m-tiles
     (100, 768, 256, 128, False),
     (128, 1024, 384, 128, True),
     (200, 512, 1280, 128, False),

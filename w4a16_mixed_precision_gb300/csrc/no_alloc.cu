@@ -57,14 +57,12 @@ extern "C" marlin_status_t marlin_gemm_no_alloc(const uint16_t* X, const void* p
   if (need > kScratchBytes) return MARLIN_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;
   if ((s = scratch_on(dev, &scratch)) != MARLIN_OK) return s;
-  // The array keeps the previous call's contents.  The status word (first 256
-  // bytes) and the tile arrival counters that follow must start at zero: clear
-  // them (at most one counter per 8 tokens x 128 columns; clearing into the
-  // partial tiles is harmless, they are written before they are read).
-  size_t head = 256 + (size_t)4 * (size_t)((M + 7) / 8) * (size_t)(N / 128);
-  head = (head + 255) / 256 * 256;
-  if (head > need) head = need;
-  if (cudaMemsetAsync(scratch, 0, head, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+  // The array keeps the previous call's contents.  Everything this call uses
+  // must start at zero: the status word, the tile arrival counters, and the
+  // partial-tile words (a zero word means "not yet written").  A completed call
+  // leaves them zeroed, but one whose kernel gave up on a bounded wait may not,
+  // and this entry point does not report that; so clear the whole region.
+  if (cudaMemsetAsync(scratch, 0, need, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MARLIN_ERR_CUDA;
   return marlin_gemm(X, packed, scales, zeros, Y, M, K, N, group, scratch, kScratchBytes, stream);
 }
