@@ -100,7 +100,8 @@ marlin_status_t marlin_repack(const int32_t* q, const uint16_t* scales, const in
  * (its SM count sets the partition).  The workspace holds the fp32 partial
  * tiles of the striped partition's global reduction, one arrival counter per
  * output tile and a status word.  A buffer sized for M also serves every
- * smaller M with the same K, N, group.  Host-only; queries the device
+ * smaller M with the same K, N, group, with either kernel (marlin_gemm_ex).
+ * Host-only; queries the device
  * attributes once.  bytes: host pointer, written.
  */
 marlin_status_t marlin_workspace_bytes(int M, int K, int N, int group, int device, size_t* bytes);
@@ -131,6 +132,34 @@ marlin_status_t marlin_workspace_bytes(int M, int K, int N, int group, int devic
 marlin_status_t marlin_gemm(const uint16_t* X, const void* packed, const uint16_t* scales,
                             const int32_t* zeros, uint16_t* Y, int M, int K, int N, int group,
                             void* workspace, size_t workspace_bytes, marlin_stream_t stream);
+
+/*
+ * Which fused kernel marlin_gemm_ex launches.  The pages' kernel is one
+ * design; this build has two for the same operation: a warp-level one
+ * (mma.sync fed from registers, M <= 32) and a tcgen05 one (operand in tensor
+ * memory, any M).  MARLIN_KERNEL_AUTO picks by M (the warp-level kernel for
+ * M <= 24, or the bound set by the environment variable W4A16_SMALL_M_MAX,
+ * 0..32).
+ */
+typedef enum {
+  MARLIN_KERNEL_AUTO = 0,
+  MARLIN_KERNEL_WARP = 1,
+  MARLIN_KERNEL_TCGEN05 = 2
+} marlin_kernel_t;
+
+/*
+ * marlin_gemm with the kernel chosen by the caller (e.g. by a per-shape tuner
+ * that times both).  Same arguments, results and errors as marlin_gemm; the
+ * two kernels agree within the parity tolerance but not bit for bit (their
+ * fp32 summation orders differ).  kernel: a marlin_kernel_t; other values ->
+ * MARLIN_ERR_INVALID_ARG; MARLIN_KERNEL_WARP with M > 32 ->
+ * MARLIN_ERR_UNSUPPORTED.  A workspace sized by marlin_workspace_bytes for M
+ * serves either kernel.
+ */
+marlin_status_t marlin_gemm_ex(const uint16_t* X, const void* packed, const uint16_t* scales,
+                               const int32_t* zeros, uint16_t* Y, int M, int K, int N, int group,
+                               void* workspace, size_t workspace_bytes, marlin_kernel_t kernel,
+                               marlin_stream_t stream);
 
 /*
  * marlin_gemm without a caller-provided workspace.  The Marlin pages have no

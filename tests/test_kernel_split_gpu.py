@@ -63,3 +63,46 @@ def test_warp_level_kernel_up_to_its_largest_batch():
     cases = [(25, 1024, 640, 128, True), (32, 2048, 1024, 128, False), (31, 4096, 384, 4096, True)]
     for M, ok, err in _run(32, cases):
         assert ok, f"M={M}: max abs err {err}"
+
+
+def test_forced_kernels_and_tuner_match_the_oracle():
+    """marlin_gemm_ex with each kernel forced, on one workspace sized for M
+    (which must serve both), and the per-shape tuner's choice."""
+    import numpy as np
+
+    import oracle
+    import w4a16_mixed_precision_gb300 as w4
+    from w4a16_mixed_precision_gb300 import _binding as b
+    from w4a16_mixed_precision_gb300.tune import best_kernel, tuned_gemm_into
+    from workloads import Problem, make_inputs
+    dev = torch.device("cuda", 0)
+    for M, asym in ((5, True), (24, False), (32, True)):
+        p = Problem("forced", M, 1024, 640, 128, asym)
+        inp = make_inputs(p)
+        pw = w4.repack(torch.from_numpy(inp.Qp).to(dev), torch.from_numpy(inp.S).to(dev),
+                       torch.from_numpy(inp.Zp).to(dev) if asym else None, 128)
+        ws = w4.Workspace(M, p.K, p.N, 128)
+        x = torch.from_numpy(inp.X).to(dev)
+        ref = oracle.w4a16(inp.X, inp.Qp, inp.S, inp.Zp, 128, p.N)
+        for k in ("warp", "tcgen05"):
+            y = torch.empty((M, p.N), dtype=torch.float16, device=dev)
+            w4.gemm_into(x, pw, ws, y, kernel=k)
+            torch.cuda.synchronize()
+            assert w4.device_status(ws) == 0
+            ok, err, _ = oracle.within_tolerance(y.cpu().numpy(), ref)
+            assert ok, f"M={M} kernel={k}: max abs err {err}"
+        assert best_kernel(x, pw, ws) in ("warp", "tcgen05")
+        y = torch.empty((M, p.N), dtype=torch.float16, device=dev)
+        tuned_gemm_into(x, pw, ws, y)
+        torch.cuda.synchronize()
+        ok, err, _ = oracle.within_tolerance(y.cpu().numpy(), ref)
+        assert ok
+    # the warp-level kernel has no M > 32 variant; an unknown kernel id is rejected
+    ws = w4.Workspace(40, 1024, 640, 128)
+    x = torch.zeros((40, 1024), dtype=torch.float16, device=dev)
+    y = torch.empty((40, 640), dtype=torch.float16, device=dev)
+    assert b.gemm_ex_raw(x.data_ptr(), pw.codes_ptr, pw.scales_ptr, None, y.data_ptr(), 40, 1024, 640, 128,
+                         ws.ptr, ws.nbytes, 1, 0) == b.ERR_UNSUPPORTED
+    assert b.gemm_ex_raw(x.data_ptr(), pw.codes_ptr, pw.scales_ptr, None, y.data_ptr(), 40, 1024, 640, 128,
+                         ws.ptr, ws.nbytes, 7, 0) == b.ERR_INVALID_ARG
+    assert np.isfinite(1.0)

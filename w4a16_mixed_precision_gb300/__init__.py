@@ -102,15 +102,21 @@ class Workspace:
         return self.buf.data_ptr()
 
 
-def gemm_into(x: torch.Tensor, w: PackedWeights, ws: Workspace, y: torch.Tensor) -> torch.Tensor:
-    """y[M, N] = x[M, K] . dequant(W), fp16, on the current stream."""
+def gemm_into(x: torch.Tensor, w: PackedWeights, ws: Workspace, y: torch.Tensor,
+              kernel: str = "auto") -> torch.Tensor:
+    """y[M, N] = x[M, K] . dequant(W), fp16, on the current stream.  kernel:
+    "auto" (by M), "warp" (warp-level kernel, M <= 32) or "tcgen05"."""
     _need_cuda(x, "x", torch.float16)
     _need_cuda(y, "y", torch.float16)
     M, K = x.shape
     if K != w.K or tuple(y.shape) != (M, w.N):
         raise ValueError("shape mismatch")
-    rc = _binding.gemm_raw(x.data_ptr(), w.codes_ptr, w.scales_ptr, w.zeros_ptr, y.data_ptr(), M, K,
-                           w.N, w.group, ws.ptr, ws.nbytes, _stream())
+    if kernel == "auto":
+        rc = _binding.gemm_raw(x.data_ptr(), w.codes_ptr, w.scales_ptr, w.zeros_ptr, y.data_ptr(), M, K,
+                               w.N, w.group, ws.ptr, ws.nbytes, _stream())
+    else:
+        rc = _binding.gemm_ex_raw(x.data_ptr(), w.codes_ptr, w.scales_ptr, w.zeros_ptr, y.data_ptr(), M,
+                                  K, w.N, w.group, ws.ptr, ws.nbytes, _binding.KERNELS[kernel], _stream())
     if rc != _binding.OK:
         raise MarlinError(rc, "marlin_gemm")
     return y

@@ -29,6 +29,7 @@ EXPORTS = (
     "marlin_repack",
     "marlin_workspace_bytes",
     "marlin_gemm",
+    "marlin_gemm_ex",
     "marlin_gemm_no_alloc",
     "marlin_gemm_host",
     "marlin_last_device_status",
@@ -64,6 +65,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.marlin_repack.argtypes = [P, P, P, I, I, I, P, P]
         lib.marlin_workspace_bytes.argtypes = [I, I, I, I, I, ctypes.POINTER(SZ)]
         lib.marlin_gemm.argtypes = [P, P, P, P, P, I, I, I, I, P, SZ, P]
+        lib.marlin_gemm_ex.argtypes = [P, P, P, P, P, I, I, I, I, P, SZ, I, P]
+        lib.marlin_gemm_ex.restype = I
         lib.marlin_last_device_status.argtypes = [P, P]
         lib.marlin_gemm_no_alloc.argtypes = [P, P, P, P, P, I, I, I, I, P]
         lib.marlin_gemm_no_alloc.restype = I
@@ -112,6 +115,16 @@ def gemm_raw(x_ptr: int, packed_ptr: int, scales_ptr: int, zeros_ptr: int | None
     """Raw call; returns the status code."""
     return load().marlin_gemm(x_ptr, packed_ptr, scales_ptr, zeros_ptr or None, y_ptr, M, K, N,
                               group, ws_ptr, ws_bytes, stream or None)
+
+
+KERNELS = {"auto": 0, "warp": 1, "tcgen05": 2}
+
+
+def gemm_ex_raw(x_ptr: int, packed_ptr: int, scales_ptr: int, zeros_ptr: int | None, y_ptr: int, M: int,
+                K: int, N: int, group: int, ws_ptr: int, ws_bytes: int, kernel: int, stream: int) -> int:
+    """Raw call with an explicit kernel (0 auto, 1 warp-level, 2 tcgen05); returns the status code."""
+    return load().marlin_gemm_ex(x_ptr, packed_ptr, scales_ptr, zeros_ptr or None, y_ptr, M, K, N,
+                                 group, ws_ptr, ws_bytes, kernel, stream or None)
 
 
 def gemm_host_raw(xh_ptr: int, xd_ptr: int, packed_ptr: int, scales_ptr: int, zeros_ptr: int | None,

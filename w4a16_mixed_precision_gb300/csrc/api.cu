@@ -76,7 +76,7 @@ int small_m_max() {
   static int v = [] {
     const char* e = getenv("W4A16_SMALL_M_MAX");
     int x = e ? atoi(e) : 24;
-    return x < 0 ? 0 : (x > 32 ? 32 : x);
+    return x < 0 ? 0 : (x > kMaxWarpM ? kMaxWarpM : x);
   }();
   return v;
 }
@@ -101,11 +101,15 @@ int xmap_slot(const void* X, int M, int K, int bn) {
 // The partition plan.  A unit is one (m-tile, 128-column tile, K slice of
 // cpu*64 rows); the grid is one CTA per SM (fewer if there are fewer units),
 // each taking an equal contiguous stripe of units.
-GemmPlan make_plan(int M, int K, int N, int group, int sms, int smem_optin, bool has_zeros) {
+// kernel: MARLIN_KERNEL_AUTO picks by M (small_m_max); the others force one.
+GemmPlan make_plan(int M, int K, int N, int group, int sms, int smem_optin, bool has_zeros,
+                   int kernel = MARLIN_KERNEL_AUTO) {
   GemmPlan g{};
   g.n_tiles = N / kTileN;
   const int budget = smem_optin - kCtrlBytes - 1024;  // control block + alignment slack
-  if (M <= small_m_max()) {
+  const bool warp_level =
+      kernel == MARLIN_KERNEL_WARP || (kernel == MARLIN_KERNEL_AUTO && M <= small_m_max());
+  if (warp_level) {
     // tokens in blocks of 8 (the mma.sync N dimension)
     g.kind = kKernelSmallM;
     g.bn = 8 * ((M + 7) / 8);
@@ -118,9 +122,6 @@ GemmPlan make_plan(int M, int K, int N, int group, int sms, int smem_optin, bool
     g.kind = kKernelTcgen05;
     g.bn = M <= kMaxBn ? (int)round_up((size_t)M, 16) : kMaxBn;
     g.m_tiles = (M + g.bn - 1) / g.bn;
-    // two MMA issuers (accumulators of bn columns each, one per dequant
-    // warpgroup and 64-row chunk of a 128-row unit) when both fit beside the A
-    // stages in tensor memory
     // two MMA issuers: for bn <= 128 on alternate units, each into its own
     // accumulator; above, on every unit, splitting the bn token columns of one
     // accumulator at 128 (so each issues MMAs of N <= 128)
@@ -226,13 +227,13 @@ marlin_status_t marlin_workspace_bytes(int M, int K, int N, int group, int devic
   DeviceState* d;
   marlin_status_t s = device_state(device, &d);
   if (s != MARLIN_OK) return s;
-  // the workspace must serve both kernels for every M' <= M
-  GemmPlan g = make_plan(M > 0 ? M : 1, K, N, group, d->sms, d->smem_optin, true);
-  size_t need = g.ws_bytes;
-  if (M > small_m_max() && small_m_max() > 0) {
-    const GemmPlan s = make_plan(small_m_max(), K, N, group, d->sms, d->smem_optin, true);
-    if (s.ws_bytes > need) need = s.ws_bytes;
-  }
+  // the workspace must serve either kernel for every M' <= M (its size grows
+  // with M' for each kernel; the warp-level one serves M' <= 32)
+  const int m = M > 0 ? M : 1;
+  size_t need = make_plan(m, K, N, group, d->sms, d->smem_optin, true, MARLIN_KERNEL_TCGEN05).ws_bytes;
+  const GemmPlan w = make_plan(m < kMaxWarpM ? m : kMaxWarpM, K, N, group, d->sms, d->smem_optin, true,
+                               MARLIN_KERNEL_WARP);
+  if (w.ws_bytes > need) need = w.ws_bytes;
   *bytes = need;
   return MARLIN_OK;
 }
@@ -240,7 +241,18 @@ marlin_status_t marlin_workspace_bytes(int M, int K, int N, int group, int devic
 marlin_status_t marlin_gemm(const uint16_t* X, const void* packed, const uint16_t* scales,
                             const int32_t* zeros, uint16_t* Y, int M, int K, int N, int group,
                             void* workspace, size_t workspace_bytes, marlin_stream_t stream) {
+  return marlin_gemm_ex(X, packed, scales, zeros, Y, M, K, N, group, workspace, workspace_bytes,
+                        MARLIN_KERNEL_AUTO, stream);
+}
+
+marlin_status_t marlin_gemm_ex(const uint16_t* X, const void* packed, const uint16_t* scales,
+                               const int32_t* zeros, uint16_t* Y, int M, int K, int N, int group,
+                               void* workspace, size_t workspace_bytes, marlin_kernel_t kernel,
+                               marlin_stream_t stream) {
   if (M < 0 || !valid_shape(K, N) || !normalise_group(K, &group)) return MARLIN_ERR_INVALID_ARG;
+  if (kernel != MARLIN_KERNEL_AUTO && kernel != MARLIN_KERNEL_WARP && kernel != MARLIN_KERNEL_TCGEN05)
+    return MARLIN_ERR_INVALID_ARG;
+  if (kernel == MARLIN_KERNEL_WARP && M > kMaxWarpM) return MARLIN_ERR_UNSUPPORTED;
   if (M == 0) return MARLIN_OK;
   if (!X || !packed || !scales || !Y || !workspace) return MARLIN_ERR_INVALID_ARG;
   if (!aligned16(X) || !aligned16(packed) || !aligned16(scales) || (zeros && !aligned16(zeros)) ||
@@ -253,7 +265,7 @@ marlin_status_t marlin_gemm(const uint16_t* X, const void* packed, const uint16_
   if ((s = device_state(dev, &d)) != MARLIN_OK) return s;
   if ((s = get_encoder()) != MARLIN_OK) return s;
 
-  const GemmPlan g = make_plan(M, K, N, group, d->sms, d->smem_optin, zeros != nullptr);
+  const GemmPlan g = make_plan(M, K, N, group, d->sms, d->smem_optin, zeros != nullptr, kernel);
   if (g.stages < 2 || g.units > 0x7FFFFFFFLL / 2) return MARLIN_ERR_UNSUPPORTED;
   if (g.kind == kKernelTcgen05 && g.a_slots < 4) return MARLIN_ERR_UNSUPPORTED;
   if (workspace_bytes < g.ws_bytes) return MARLIN_ERR_WORKSPACE_TOO_SMALL;

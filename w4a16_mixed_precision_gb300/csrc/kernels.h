@@ -13,6 +13,7 @@ constexpr int kThreads = 640;      // 20 warps: 2 producers, 2 MMA issuers (one 
 constexpr int kTileN = 128;        // output columns per tile = UMMA M
 constexpr int kChunkK = 64;        // K elements per dequantised A chunk
 constexpr int kChunkCodeBytes = kTileN * kChunkK / 2;  // 4096
+constexpr int kMaxWarpM = 32;      // largest M the warp-level kernel serves (4 blocks of 8 tokens)
 constexpr int kAStages = 12;       // most A slots (one unit each) resident in TMEM
 constexpr int kTmemCols = 512;
 constexpr int kMaxStages = 16;
