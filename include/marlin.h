@@ -4,11 +4,12 @@
  *     Y[M][N] = X[M][K] . dequant(W)[K][N],   dequant(w) = fp16((q - z) * s)
  *
  * The operation is the one the Marlin pages define: "Marlin / GPTQ-Marlin"
- * (brain.gartu.xyz), section "Le probleme": every linear layer computes
+ * (brain.gartu.xyz), section "Le problème": every linear layer computes
  * Y = X_fp16 x W_int4, the INT4 weights dequantised to FP16 on the fly;
- * "Marlin" (dingiv.github.io), section "Group size": one fp16 scale (and one
- * zero point) per group of 128 consecutive K elements of a column; section
- * "dequant precision": FP16 operands, FP32 accumulation, FP16 output.
+ * "Marlin" (dingiv.github.io), section "Group size 为什么是 128": one fp16
+ * scale (and one zero point) per group of 128 consecutive K elements of a
+ * column; section "反量化精度权衡": FP16 operands, FP32 accumulation, FP16
+ * output.
  *
  * Conventions for every entry point
  *   - Device pointers are CUDA device addresses on the current device; host
@@ -109,7 +110,7 @@ marlin_status_t marlin_workspace_bytes(int M, int K, int N, int group, int devic
 /*
  * The fused W4A16 matrix multiply: Y = X . dequant(W) with fp32 accumulation
  * and fp16 output (round to nearest even; overflow gives +-inf).
- * "Marlin / GPTQ-Marlin", sections "Le probleme" and "Architecture generale"
+ * "Marlin / GPTQ-Marlin", sections "Le problème" and "Architecture générale"
  * (one kernel fuses the dequantisation and the GEMM); "Marlin Project
  * Overview", section "Key Techniques", item "Striped Partitioning" (the SM
  * partition with global reduction).

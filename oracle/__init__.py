@@ -9,10 +9,10 @@ The arithmetic lives in ``oracle.c`` (plain C, binary64, no FMA contraction).
 This module only builds it, loads it with ctypes and marshals numpy arrays.
 Definitions followed (page titles and sections):
 
-* "Marlin / GPTQ-Marlin", section "Le probleme": ``Y = X_fp16 x W_int4`` with the
+* "Marlin / GPTQ-Marlin", section "Le problème": ``Y = X_fp16 x W_int4`` with the
   INT4 weights dequantised to FP16 before the multiply.
-* "Marlin" (dingiv.github.io), section "Group size": one scale and one zero point
-  per 128 consecutive weights; section "dequant precision": INT4 -> FP16 is
+* "Marlin" (dingiv.github.io), section "Group size 为什么是 128": one scale and one zero point
+  per 128 consecutive weights; section "反量化精度权衡": INT4 -> FP16 is
   exact, accumulation is FP32 inside the tensor core, output is FP16.
 """
 from __future__ import annotations

@@ -8,12 +8,12 @@
  * CUDA library.
  *
  * What it follows (pages on Marlin, cited by title and section):
- *   - "Marlin / GPTQ-Marlin" (brain.gartu.xyz), section "Le probleme": each
+ *   - "Marlin / GPTQ-Marlin" (brain.gartu.xyz), section "Le problème": each
  *     linear layer computes Y = X_fp16 x W_int4, dequantising the INT4 weights
  *     to FP16 on the fly before the multiply.
- *   - "Marlin" (dingiv.github.io), section "Group size": one scale (and one
+ *   - "Marlin" (dingiv.github.io), section "Group size 为什么是 128": one scale (and one
  *     zero point) per group of 128 consecutive weights.
- *   - same page, section "dequant precision": INT4 -> FP16 is exact (FP16 holds
+ *   - same page, section "反量化精度权衡": INT4 -> FP16 is exact (FP16 holds
  *     all 16 values), the multiply accumulates in FP32 and the output is FP16.
  *
  * The oracle computes the plain definition, with no blocking or reordering:
@@ -25,7 +25,7 @@
  *   4. y[m][n] = sum_k x[m][k] * w[k][n], in binary64, k ascending
  * plus the tile layout of the repacked weights (the "reshuffle" of the pages:
  * "Marlin / GPTQ-Marlin", section "Tiled layout et repacking"; "Marlin Project
- * Overview" (vecbase.com), section "Key Techniques", item "Reshuffling").  The
+ * Overview" (vecbase.com), section "Key Techniques", item "Reshuffling for Access Patterns").  The
  * repacked layout is this library's own, the operand order of a 16x16 fp16
  * tensor-core fragment; its index formula is:
  *   codes: word ((nt*(K/64) + kb)*8 + g)*128 + l*4 + j   (nt < N/128, kb < K/64,

@@ -1,8 +1,8 @@
 // gemm.cu -- the fused W4A16 matrix multiply for GB300 (sm_103a).
 //
 // Computes Y[M][N] = X[M][K] . dequant(W)[K][N], dequant(w) = fp16((q - z) * s)
-// ("Marlin / GPTQ-Marlin", section "Le probleme"; "Marlin" (dingiv.github.io),
-// sections "Group size" and "dequant precision").
+// ("Marlin / GPTQ-Marlin", section "Le problème"; "Marlin" (dingiv.github.io),
+// sections "Group size 为什么是 128" and "反量化精度权衡").
 //
 // Design (Blackwell-first; the pages' Ampere kernel is prior art only):
 //   * Swapped operands: the tensor core computes D[n][m] = sum_k Wt[n][k] X[m][k]
@@ -15,9 +15,9 @@
 //     the tile's first unit, in a fixed order, so results are bit-reproducible.
 //   * Warp roles: warp 0 streams packed codes, scales, zeros (bulk TMA) and
 //     warp 3 streams X (tensor TMA, 128-byte swizzle) through a multi-stage
-//     mbarrier ring in shared memory ("Marlin", section "async copy and
-//     pipeline"); warps 4..19 (four warpgroups, taking whole units in turn)
-//     turn 4-bit codes into fp16 with the 0x6400 exponent trick, scale them
+//     mbarrier ring in shared memory ("Marlin", sections "异步内存拷贝" and
+//     "Striped 划分与流水线"); warps 4..19 (four warpgroups, taking whole
+//     units in turn) turn 4-bit codes into fp16 with the 0x6400 exponent trick, scale them
 //     with one fp16 multiply, and store the result straight into tensor memory
 //     as the A operand; warps 1 and 2 issue tcgen05.mma (A from TMEM, B = X
 //     from shared memory, fp32 accumulators in TMEM): for bn <= 128 on

@@ -1,7 +1,7 @@
 // repack.cu -- offline rewrite of GPTQ-order 4-bit codes, scales and zeros into
 // the layout the fused kernels stream ("Marlin / GPTQ-Marlin", section "Tiled
 // layout et repacking": done once at load time; "Marlin Project Overview",
-// section "Key Techniques", item "Reshuffling": weights and scales rearranged
+// section "Key Techniques", item "Reshuffling for Access Patterns": weights and scales rearranged
 // offline into tensor-core operand order).
 //
 // Code layout: for every 128-column tile nt and 64-row block kb, one 4 KB chunk
