@@ -48,6 +48,10 @@ SMALL_CASES = [
     (200, 512, 1280, 128, False),
     (256, 512, 384, 128, False),
     (257, 512, 256, 128, True),        # two m-tiles, 1-row tail
+    (129, 512, 384, 256, False),       # bn = 144: the second issuer's columns are N = 16
+    (256, 1024, 512, 128, True),       # bn = 256 exactly, explicit zeros
+    (1, 128, 128, 128, True),          # one unit, one tile, explicit zeros
+    (40, 128, 256, 128, False),        # K of a single 128-row unit on the tcgen05 kernel
     (600, 1024, 512, 128, False),
 ]
 
