@@ -76,8 +76,15 @@ def _load():
         lib.oracle_round_array.restype = None
         lib.oracle_widen_array.argtypes = [P, ctypes.c_int64, P]
         lib.oracle_widen_array.restype = None
+        lib.oracle_sparse_compress.argtypes = [P, P, I, I, I, P, P]
+        lib.oracle_sparse_expand.argtypes = [P, P, P, I, I, I, P]
+        lib.oracle_w4a16_sparse.argtypes = [P, P, P, P, P, I, I, I, I, P, ctypes.c_int64, P, I]
+        lib.oracle_sparse_repack.argtypes = [P, P, I, I, P, P]
+        lib.oracle_sparse_unrepack.argtypes = [P, P, I, I, P, P]
         for name in ("oracle_unpack_codes", "oracle_unpack_zeros", "oracle_dequant", "oracle_gemm",
-                     "oracle_w4a16", "oracle_repack", "oracle_unrepack"):
+                     "oracle_w4a16", "oracle_repack", "oracle_unrepack", "oracle_sparse_compress",
+                     "oracle_sparse_expand", "oracle_w4a16_sparse", "oracle_sparse_repack",
+                     "oracle_sparse_unrepack"):
             getattr(lib, name).restype = I
         _lib = lib
         return lib
@@ -215,6 +222,75 @@ def unrepack(P, K: int, N: int) -> np.ndarray:
     Qp = np.empty((K // 8, N), np.int32)
     assert _load().oracle_unrepack(_ptr(P), K, N, _ptr(Qp)) == 0
     return Qp
+
+
+# ---- 2:4 structured sparsity ("Marlin", section "支持 2:4 稀疏加速"; "Marlin /
+# GPTQ-Marlin", section "4. Support de la sparsité 2:4 NVIDIA") ----------------
+
+def sparse_compress(Qp, Zp, K: int, N: int, g: int):
+    """GPTQ-order codes -> (kc uint8 [K/2][N], ki uint8 [K/4][N], bad groups).
+
+    Per group of four rows 4j..4j+3 of column n: kept positions i0 < i1 (the
+    codes that differ from the zero point, completed with the lowest positions
+    whose code equals it), kc[2j+t][n] = code at i_t, ki[j][n] = i0 | i1 << 2.
+    bad = groups where more than two codes differ from the zero point.
+    """
+    Qp, Zp = _i32(Qp), _i32(Zp)
+    kc = np.empty((K // 2, N), np.uint8)
+    ki = np.empty((K // 4, N), np.uint8)
+    bad = _load().oracle_sparse_compress(_ptr(Qp), _ptr(Zp), K, N, g, _ptr(kc), _ptr(ki))
+    assert bad >= 0
+    return kc, ki, int(bad)
+
+
+def sparse_expand(kc, ki, Zp, K: int, N: int, g: int) -> np.ndarray:
+    """Compressed form -> dense GPTQ-order int32 [K/8][N] (zero point at dropped rows)."""
+    kc = np.ascontiguousarray(kc, np.uint8)
+    ki = np.ascontiguousarray(ki, np.uint8)
+    Zp = _i32(Zp)
+    Qp = np.empty((K // 8, N), np.int32)
+    assert _load().oracle_sparse_expand(_ptr(kc), _ptr(ki), _ptr(Zp), K, N, g, _ptr(Qp)) == 0
+    return Qp
+
+
+def w4a16_sparse(X, kc, ki, S, Zp, g: int, N: int, idx=None, threads: int | None = None) -> np.ndarray:
+    """binary64 Y = X . dequant(W) for 2:4 weights, summing the kept terms only."""
+    X, S, Zp = _bits16(X), _bits16(S), _i32(Zp)
+    kc = np.ascontiguousarray(kc, np.uint8)
+    ki = np.ascontiguousarray(ki, np.uint8)
+    M, K = X.shape
+    if idx is None:
+        out = np.empty((M, N), np.float64)
+        count, idx_p = 0, None
+    else:
+        idx = np.ascontiguousarray(np.asarray(idx, dtype=np.int64))
+        out = np.empty(idx.shape[0], np.float64)
+        count, idx_p = idx.shape[0], _ptr(idx)
+    rc = _load().oracle_w4a16_sparse(_ptr(X), _ptr(kc), _ptr(ki), _ptr(S), _ptr(Zp), M, K, N, g,
+                                     idx_p, count, _ptr(out), _threads(threads))
+    assert rc == 0
+    return out
+
+
+def sparse_repack(kc, ki, K: int, N: int):
+    """Compressed form -> this library's sparse tile layout: (codes int32
+    [(N/128)*(K/64)*512], meta int32 [(N/128)*(K/64)*256])."""
+    kc = np.ascontiguousarray(kc, np.uint8)
+    ki = np.ascontiguousarray(ki, np.uint8)
+    blocks = (N // 128) * (K // 64)
+    Pc = np.empty(blocks * 512, np.int32)
+    Pm = np.empty(blocks * 256, np.int32)
+    assert _load().oracle_sparse_repack(_ptr(kc), _ptr(ki), K, N, _ptr(Pc), _ptr(Pm)) == 0
+    return Pc, Pm
+
+
+def sparse_unrepack(Pc, Pm, K: int, N: int):
+    """Inverse of sparse_repack: (kc, ki)."""
+    Pc, Pm = _i32(Pc), _i32(Pm)
+    kc = np.empty((K // 2, N), np.uint8)
+    ki = np.empty((K // 4, N), np.uint8)
+    assert _load().oracle_sparse_unrepack(_ptr(Pc), _ptr(Pm), K, N, _ptr(kc), _ptr(ki)) == 0
+    return kc, ki
 
 
 def to_half_rne(y) -> np.ndarray:

@@ -36,6 +36,11 @@
  *   zeros:  bytes [N/128][K/g][64], the 64-byte slice Zp[gi][16*(n/128) .. +15]
  *           at ((n/128)*(K/g) + gi)*64.
  *
+ * 2:4 structured sparsity ("Marlin", section "支持 2:4 稀疏加速"; "Marlin /
+ * GPTQ-Marlin", section "4. Support de la sparsité 2:4 NVIDIA"): the compressed
+ * form of 2:4 codes, its inverse, the product over the kept terms only, and
+ * the library's sparse tile layout (section "2:4 structured sparsity" below).
+ *
  * Build: gcc -O2 -ffp-contract=off -fPIC -shared -pthread (no FMA contraction,
  * so every sum rounds after each add, identically on x86-64 and aarch64).
  */
@@ -319,6 +324,220 @@ int oracle_repack_zeros(const int32_t* Zp, int G, int N, uint8_t* out) {
       if (n % 2 == 0) *b = (uint8_t)((*b & 0xF0) | z);
       else *b = (uint8_t)((*b & 0x0F) | (z << 4));
     }
+  return 0;
+}
+
+/* ---- 2:4 structured sparsity ---------------------------------------------
+ *
+ * "Marlin" (dingiv.github.io), section "支持 2:4 稀疏加速": in every four
+ * weights two are zero, at positions fixed ahead of inference; "Marlin /
+ * GPTQ-Marlin" (brain.gartu.xyz), section "4. Support de la sparsité 2:4
+ * NVIDIA": the zeros are skipped after dequantisation and the sparse tensor
+ * core multiplies only the kept half.
+ *
+ * Readings (the pages fix neither): a dequantised weight is zero exactly when
+ * its code equals its zero point z (w = (q - z)*s); the four weights of a group
+ * are four consecutive rows k = 4j .. 4j+3 of one column n, i.e. along the
+ * reduction, which is the direction the sparse tensor core compresses.
+ *
+ * Compressed form, for every (j, n): kept positions i0 < i1 in 0..3 are the
+ * positions whose code differs from z, in ascending order, completed (when
+ * there are fewer than two) with the lowest positions whose code equals z; the
+ * kept codes are c_t = q[4j + i_t][n].  Stored as kc[(2j + t)*N + n] = c_t and
+ * ki[j*N + n] = i0 | (i1 << 2).  A group with three or four codes that differ
+ * from z is not 2:4; it is counted and keeps its first two such positions.
+ *
+ * The sparse product is the dense one on the expanded codes, since every
+ * dropped weight dequantises to exactly zero; oracle_w4a16_sparse sums only
+ * the kept terms, j ascending and i0 before i1, i.e. k ascending. */
+
+static inline int zero_for(const int32_t* Zp, int N, int g, int k, int n) {
+  return zero_at(Zp, N, k / g, n);
+}
+
+int oracle_sparse_compress(const int32_t* Qp, const int32_t* Zp, int K, int N, int g, uint8_t* kc,
+                           uint8_t* ki) {
+  if (K <= 0 || N <= 0 || K % 8 || N % 8 || g <= 0 || K % g || g % 4) return -1;
+  int bad = 0;
+  for (int j = 0; j < K / 4; ++j)
+    for (int n = 0; n < N; ++n) {
+      int z = zero_for(Zp, N, g, 4 * j, n);
+      int pos[4], cnt = 0;
+      for (int i = 0; i < 4; ++i)
+        if (code_at(Qp, N, 4 * j + i, n) != z && cnt < 2) pos[cnt++] = i;
+      int nz = 0;
+      for (int i = 0; i < 4; ++i) nz += code_at(Qp, N, 4 * j + i, n) != z;
+      if (nz > 2) ++bad;
+      /* complete with the lowest positions not yet taken */
+      for (int i = 0; i < 4 && cnt < 2; ++i) {
+        int taken = 0;
+        for (int c = 0; c < cnt; ++c) taken |= pos[c] == i;
+        if (!taken) pos[cnt++] = i;
+      }
+      if (pos[0] > pos[1]) { int t = pos[0]; pos[0] = pos[1]; pos[1] = t; }
+      kc[(size_t)(2 * j) * N + n] = (uint8_t)code_at(Qp, N, 4 * j + pos[0], n);
+      kc[(size_t)(2 * j + 1) * N + n] = (uint8_t)code_at(Qp, N, 4 * j + pos[1], n);
+      ki[(size_t)j * N + n] = (uint8_t)(pos[0] | (pos[1] << 2));
+    }
+  return bad;
+}
+
+/* Dense GPTQ-order codes from the compressed form: z at the dropped rows. */
+int oracle_sparse_expand(const uint8_t* kc, const uint8_t* ki, const int32_t* Zp, int K, int N, int g,
+                         int32_t* Qp) {
+  if (K <= 0 || N <= 0 || K % 8 || N % 8 || g <= 0 || K % g || g % 4) return 1;
+  memset(Qp, 0, sizeof(int32_t) * (size_t)(K / 8) * N);
+  for (int j = 0; j < K / 4; ++j)
+    for (int n = 0; n < N; ++n) {
+      int i0 = ki[(size_t)j * N + n] & 3, i1 = (ki[(size_t)j * N + n] >> 2) & 3;
+      if (i0 >= i1) return 2;
+      for (int i = 0; i < 4; ++i) {
+        int k = 4 * j + i;
+        int q = zero_for(Zp, N, g, k, n);
+        if (i == i0) q = kc[(size_t)(2 * j) * N + n];
+        if (i == i1) q = kc[(size_t)(2 * j + 1) * N + n];
+        Qp[(size_t)(k / 8) * N + n] |= (int32_t)((uint32_t)(q & 0xF) << (4 * (k % 8)));
+      }
+    }
+  return 0;
+}
+
+typedef struct {
+  const uint16_t* X;
+  const uint8_t *kc, *ki;
+  const uint16_t* S;
+  const int32_t* Zp;
+  int M, K, N, g;
+  const int64_t* idx;
+  int64_t i0, i1;
+  double* out;
+} sparse_job;
+
+static double sparse_entry(const sparse_job* j, int m, int n) {
+  const uint16_t* x = j->X + (size_t)m * j->K;
+  double acc = 0.0;
+  for (int jj = 0; jj < j->K / 4; ++jj) {
+    uint8_t code_idx = j->ki[(size_t)jj * j->N + n];
+    for (int t = 0; t < 2; ++t) {
+      int k = 4 * jj + ((code_idx >> (2 * t)) & 3);
+      int grp = k / j->g;
+      uint16_t w = dequant_one(j->kc[(size_t)(2 * jj + t) * j->N + n], zero_at(j->Zp, j->N, grp, n),
+                               j->S[(size_t)grp * j->N + n]);
+      acc += oracle_half_to_double(x[k]) * oracle_half_to_double(w);
+    }
+  }
+  return acc;
+}
+
+static void* sparse_worker(void* arg) {
+  sparse_job* j = (sparse_job*)arg;
+  if (j->idx) {
+    for (int64_t i = j->i0; i < j->i1; ++i) {
+      int64_t f = j->idx[i];
+      j->out[i] = sparse_entry(j, (int)(f / j->N), (int)(f % j->N));
+    }
+  } else {
+    for (int64_t n = j->i0; n < j->i1; ++n)
+      for (int m = 0; m < j->M; ++m) j->out[(size_t)m * j->N + n] = sparse_entry(j, m, (int)n);
+  }
+  return NULL;
+}
+
+/* Y (or the listed entries) of X . dequant(W) for 2:4 weights in compressed
+ * form, summing the kept terms only. */
+int oracle_w4a16_sparse(const uint16_t* X, const uint8_t* kc, const uint8_t* ki, const uint16_t* S,
+                        const int32_t* Zp, int M, int K, int N, int g, const int64_t* idx,
+                        int64_t count, double* out, int nthreads) {
+  if (M < 0 || K <= 0 || N <= 0 || K % 8 || N % 8 || g <= 0 || K % g || g % 4) return 1;
+  if (M == 0) return 0;
+  int64_t total = idx ? count : N;
+  if (total <= 0) return 0;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > total) nthreads = (int)total;
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * nthreads);
+  sparse_job* jobs = (sparse_job*)malloc(sizeof(sparse_job) * nthreads);
+  for (int t = 0; t < nthreads; ++t) {
+    jobs[t] = (sparse_job){X, kc, ki, S, Zp, M, K, N, g, idx, total * t / nthreads,
+                           total * (t + 1) / nthreads, out};
+    pthread_create(&th[t], NULL, sparse_worker, &jobs[t]);
+  }
+  for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+  free(th);
+  free(jobs);
+  return 0;
+}
+
+/* The library's tile layout of the compressed form (its own: the operand
+ * order of the sparse 16x32 fp16 tensor-core fragment).  Per 128-column tile
+ * nt and 64-row block kb (16 groups of four rows):
+ *   codes: word ((nt*(K/64) + kb)*8 + gq)*64 + l*2 + s  (gq < 8, l < 32, s < 2)
+ *          holds at bits 4p..4p+3 (p < 8) the kept code c_t(j, n) with
+ *          n = nt*128 + 16gq + l/4 + 8*(p & 1),
+ *          j = kb*16 + 8s + l%4 + 4*((p >> 1) & 1),   t = p >> 2;
+ *   meta:  word ((nt*(K/64) + kb)*8 + gq)*32 + (r*2 + h)*2 + s  (r < 8, h < 2, s < 2)
+ *          holds at bits 4i..4i+3 (i < 8) the index nibble ki(j, n) with
+ *          n = nt*128 + 16gq + r + 8*(i >> 2),   j = kb*16 + 8s + 4h + (i & 3). */
+static inline int sp_code_n(int nt, int gq, int l, int p) { return nt * 128 + 16 * gq + l / 4 + 8 * (p & 1); }
+static inline int sp_code_j(int kb, int l, int s, int p) { return kb * 16 + 8 * s + l % 4 + 4 * ((p >> 1) & 1); }
+static inline int sp_meta_n(int nt, int gq, int r, int i) { return nt * 128 + 16 * gq + r + 8 * (i >> 2); }
+static inline int sp_meta_j(int kb, int h, int s, int i) { return kb * 16 + 8 * s + 4 * h + (i & 3); }
+
+int oracle_sparse_repack(const uint8_t* kc, const uint8_t* ki, int K, int N, int32_t* Pc, int32_t* Pm) {
+  if (K <= 0 || N <= 0 || K % 64 || N % 128) return 1;
+  int KB = K / 64, NT = N / 128;
+  for (int nt = 0; nt < NT; ++nt)
+    for (int kb = 0; kb < KB; ++kb)
+      for (int gq = 0; gq < 8; ++gq) {
+        size_t blk = (size_t)(nt * KB + kb) * 8 + gq;
+        for (int l = 0; l < 32; ++l)
+          for (int s = 0; s < 2; ++s) {
+            uint32_t word = 0;
+            for (int p = 0; p < 8; ++p) {
+              int n = sp_code_n(nt, gq, l, p), j = sp_code_j(kb, l, s, p);
+              word |= (uint32_t)(kc[(size_t)(2 * j + (p >> 2)) * N + n] & 0xF) << (4 * p);
+            }
+            Pc[blk * 64 + (size_t)l * 2 + s] = (int32_t)word;
+          }
+        for (int r = 0; r < 8; ++r)
+          for (int h = 0; h < 2; ++h)
+            for (int s = 0; s < 2; ++s) {
+              uint32_t word = 0;
+              for (int i = 0; i < 8; ++i) {
+                int n = sp_meta_n(nt, gq, r, i), j = sp_meta_j(kb, h, s, i);
+                word |= (uint32_t)(ki[(size_t)j * N + n] & 0xF) << (4 * i);
+              }
+              Pm[blk * 32 + (size_t)(r * 2 + h) * 2 + s] = (int32_t)word;
+            }
+      }
+  return 0;
+}
+
+/* Inverse of oracle_sparse_repack. */
+int oracle_sparse_unrepack(const int32_t* Pc, const int32_t* Pm, int K, int N, uint8_t* kc, uint8_t* ki) {
+  if (K <= 0 || N <= 0 || K % 64 || N % 128) return 1;
+  int KB = K / 64, NT = N / 128;
+  for (int nt = 0; nt < NT; ++nt)
+    for (int kb = 0; kb < KB; ++kb)
+      for (int gq = 0; gq < 8; ++gq) {
+        size_t blk = (size_t)(nt * KB + kb) * 8 + gq;
+        for (int l = 0; l < 32; ++l)
+          for (int s = 0; s < 2; ++s) {
+            uint32_t word = (uint32_t)Pc[blk * 64 + (size_t)l * 2 + s];
+            for (int p = 0; p < 8; ++p) {
+              int n = sp_code_n(nt, gq, l, p), j = sp_code_j(kb, l, s, p);
+              kc[(size_t)(2 * j + (p >> 2)) * N + n] = (uint8_t)((word >> (4 * p)) & 0xF);
+            }
+          }
+        for (int r = 0; r < 8; ++r)
+          for (int h = 0; h < 2; ++h)
+            for (int s = 0; s < 2; ++s) {
+              uint32_t word = (uint32_t)Pm[blk * 32 + (size_t)(r * 2 + h) * 2 + s];
+              for (int i = 0; i < 8; ++i) {
+                int n = sp_meta_n(nt, gq, r, i), j = sp_meta_j(kb, h, s, i);
+                ki[(size_t)j * N + n] = (uint8_t)((word >> (4 * i)) & 0xF);
+              }
+            }
+      }
   return 0;
 }
 

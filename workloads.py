@@ -12,6 +12,9 @@ Input recipe (the workloads of the pages' GEMM benchmarks, synthesised):
                                                            code of row 8r+i at nibble i)
   S  = fp16(0.02 * U(0.5, 1.5))              [K/g][N]
   Zp = uniform random 32-bit words           [K/g][N/8] (explicit zeros) or None (z = 8)
+2:4-sparse weights (make_sparse_weights): in every four consecutive rows of a
+column two positions (uniform among the six pairs) hold uniform codes and the
+other two the zero point.
 Seed = CRC32 of "cfg:M:K:N:g:asym" (see seed_for).
 """
 from __future__ import annotations
@@ -82,6 +85,36 @@ def make_weights(K: int, N: int, group: int, asym: bool, seed: int):
     Zp = None
     if asym:
         Zp = rng.integers(0, 2**32, size=(K // group, N // 8), dtype=np.uint64).astype(np.uint32).view(np.int32)
+    return Qp, S, Zp
+
+
+# the six ways to keep two of four positions, in ascending order
+_PAIRS0 = np.array([0, 0, 0, 1, 1, 2], np.uint8)
+_PAIRS1 = np.array([1, 2, 3, 2, 3, 3], np.uint8)
+
+
+def make_sparse_weights(K: int, N: int, group: int, asym: bool, seed: int):
+    """Weight-side inputs (Qp, S, Zp) of a 2:4-sparse K x N layer.
+
+    In every four consecutive rows of a column, two positions (one of the six
+    pairs, uniformly) get codes drawn uniformly from 0..15; the other two get
+    the column's zero point (8, or the drawn zero), so at most two of every
+    four weights are non-zero.  Scales as in make_weights.
+    """
+    rng = np.random.default_rng(seed)
+    G = K // group
+    z = rng.integers(0, 16, size=(G, N), dtype=np.uint8) if asym else np.full((G, N), 8, np.uint8)
+    pair = rng.integers(0, 6, size=(K // 4, N), dtype=np.uint8)
+    i0, i1 = _PAIRS0[pair], _PAIRS1[pair]
+    v0 = rng.integers(0, 16, size=(K // 4, N), dtype=np.uint8)
+    v1 = rng.integers(0, 16, size=(K // 4, N), dtype=np.uint8)
+    zr = np.repeat(z, group // 4, axis=0)  # zero point of each group of four rows
+    q = np.empty((K // 4, 4, N), np.uint8)
+    for i in range(4):
+        q[:, i, :] = np.where(i0 == i, v0, np.where(i1 == i, v1, zr))
+    Qp = pack_codes(q.reshape(K, N))
+    S = (0.02 * rng.uniform(0.5, 1.5, size=(G, N))).astype(np.float16)
+    Zp = pack_zeros(z) if asym else None
     return Qp, S, Zp
 
 
