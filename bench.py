@@ -33,7 +33,8 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from workloads import ALL_CONFIGS, Problem, make_activations, make_weights, seed_for  # noqa: E402
+from workloads import (ALL_CONFIGS, SPARSE_CONFIGS, Problem, make_activations,  # noqa: E402
+                       make_sparse_weights, make_weights, seed_for)
 
 METRIC = "W4A16 GEMM µs, HBM GB/s & TFLOP/s (% roofline) vs M; speedup over FP16 GEMM"
 WORKLOAD_NAMES = {
@@ -43,6 +44,8 @@ WORKLOAD_NAMES = {
     "70b-decode": "llama2-70b batched decode (K,N) in {8192x10240, 8192x8192, 8192x57344, 28672x8192}, "
                   "M in {1,4,16,32,64,128}, group 128, z=8",
     "prefill": "prefill M in {1024,4096,8192} x (K,N) in {8192x8192, 8192x28672}, group 128, z=8",
+    "sparse-7b-decode": "llama2-7b-decode-linears (K,N) in {4096x12288, 4096x4096, 4096x22016, 11008x4096} "
+                        "with 2:4-sparse weights (sparse path), M in {1,2,4,8,16,32}, group 128, z=8",
     "asym-odd": "asymmetric zeros, group 128 and per-column, (K,N) in {2048x2048, 2048x5632, 5120x15360, "
                 "13824x5120}, M in {1,16,48}",
 }
@@ -74,7 +77,10 @@ def kernel_source_digest() -> str:
 
 def kernel_names(problems) -> str:
     """The fused kernels a workload launches: the warp-level path for M <= 24,
-    the tcgen05 path above (the library's default split)."""
+    the tcgen05 path above (the library's default split); 2:4 weights: the
+    sparse instantiation of the warp-level kernel at every M <= 32."""
+    if any(p.sparse for p in problems):
+        return "w4a16_small_m_kernel (2:4-sparse instantiation, mma.sp)"
     small = any(p.M <= 24 for p in problems)
     big = any(p.M > 24 for p in problems)
     return " + ".join(n for n, on in (("w4a16_small_m_kernel", small), ("w4a16_gemm_kernel", big)) if on)
@@ -218,15 +224,26 @@ class OracleSampler:
 
     def inputs(self, p):
         if p.key not in self.cache:
-            Qp, S, Zp = make_weights(p.K, p.N, p.group, p.asym, seed_for(p.key))
+            if p.sparse:
+                Qp, S, Zp = make_sparse_weights(p.K, p.N, p.group, p.asym, seed_for(p.key))
+                kc, ki, _ = self.oracle.sparse_compress(Qp, Zp, p.K, p.N, p.group)
+                Qp = (kc, ki)
+            else:
+                Qp, S, Zp = make_weights(p.K, p.N, p.group, p.asym, seed_for(p.key))
             X = make_activations(p.M, p.K, seed_for(p.key) + 1)
             self.cache = {p.key: (X, Qp, S, Zp)}   # keep one problem's inputs at a time
         return self.cache[p.key]
 
+    def product(self, p, X, Qp, S, Zp, idx, threads):
+        """The oracle's product for this problem: the 2:4 form sums the kept terms only."""
+        if p.sparse:
+            return self.oracle.w4a16_sparse(X, Qp[0], Qp[1], S, Zp, p.group, p.N, idx=idx, threads=threads)
+        return self.oracle.w4a16(X, Qp, S, Zp, p.group, p.N, idx=idx, threads=threads)
+
     def calibrate(self, p):
         X, Qp, S, Zp = self.inputs(p)
         t = time.perf_counter()
-        self.oracle.w4a16(X, Qp, S, Zp, p.group, p.N, idx=np.arange(p.M) * p.N, threads=1)
+        self.product(p, X, Qp, S, Zp, np.arange(p.M) * p.N, 1)
         self.sec_per_mk = max((time.perf_counter() - t) / (p.M * p.K), 1e-10)
 
     def run(self, p, budget_s: float):
@@ -240,7 +257,7 @@ class OracleSampler:
         sel = np.sort(rng.choice(p.N, cols, replace=False))
         idx = (np.arange(p.M)[:, None] * p.N + sel[None, :]).ravel()
         t = time.perf_counter()
-        self.oracle.w4a16(X, Qp, S, Zp, p.group, p.N, idx=idx, threads=self.threads)
+        self.product(p, X, Qp, S, Zp, idx, self.threads)
         dt = time.perf_counter() - t
         return p.algorithmic_bytes() * cols / p.N, dt, cols
 
@@ -298,10 +315,15 @@ def run_reference(args, problems, rank, world):
 def run_gpu(args, problems, rank, world, local):
     import torch
 
+    import dataclasses
+
     import w4a16_mixed_precision_gb300 as w4
     from w4a16_mixed_precision_gb300 import build as cuda_build
 
     cuda_build.build()
+    sparse = problems[0].sparse
+    assert all(p.sparse == sparse for p in problems)
+    call = w4.sparse_gemm_into if sparse else w4.gemm_into
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     peaks = load_peaks()
@@ -312,24 +334,34 @@ def run_gpu(args, problems, rank, world, local):
     layers = sorted({(p.K, p.N, p.group, p.asym) for p in problems})
 
     def wbytes(K, N, g, a):
-        return K * N // 2 + (K // g) * N * 2 + ((K // g) * N // 2 if a else 0)
+        codes = K * N // 4 + K * N // 8 if sparse else K * N // 2
+        return codes + (K // g) * N * 2 + ((K // g) * N // 2 if a else 0)
 
     uses = {lk: sum(1 for p in problems if (p.K, p.N, p.group, p.asym) == lk) for lk in layers}
     step_wbytes = sum(wbytes(*lk) * uses[lk] for lk in layers)
     P = max(1, -(-2 * L2_BYTES // step_wbytes))
     packed = {}
+    dense_pw = {}
     for (K, N, g, a) in layers:
-        Qp, S, Zp = make_weights(K, N, g, a, seed=seed_for(f"w:{K}:{N}:{g}:{int(a)}"))
-        pw = w4.repack(torch.from_numpy(Qp).to(dev), torch.from_numpy(S).to(dev),
-                       torch.from_numpy(Zp).to(dev) if a else None, g)
+        gen = make_sparse_weights if sparse else make_weights
+        Qp, S, Zp = gen(K, N, g, a, seed=seed_for(f"w:{K}:{N}:{g}:{int(a)}"))
+        tq, ts = torch.from_numpy(Qp).to(dev), torch.from_numpy(S).to(dev)
+        tz = torch.from_numpy(Zp).to(dev) if a else None
+        pw = w4.sparse_repack(tq, ts, tz, g) if sparse else w4.repack(tq, ts, tz, g)
+        if sparse:
+            # the same weights in the dense layout, for the per-run comparison
+            dense_pw[(K, N, g, a)] = w4.repack(tq, ts, tz, g)
         copies = [pw]
         # the graphs use uses*P copies; the per-run table rotates through enough
         # copies of this one layer to stream more than two L2s between reuses
         n_copies = max(uses[(K, N, g, a)] * P, -(-2 * L2_BYTES // wbytes(K, N, g, a)) + 1)
         for _ in range(n_copies - 1):
-            copies.append(w4.PackedWeights(pw.buf.clone(), pw.K, pw.N, pw.group, pw.has_zeros,
-                                           pw.off_scales, pw.off_zeros))
+            copies.append(dataclasses.replace(pw, buf=pw.buf.clone()))
         packed[(K, N, g, a)] = copies
+        if sparse:
+            dense_pw[(K, N, g, a)] = [dense_pw[(K, N, g, a)]] + [
+                dataclasses.replace(dense_pw[(K, N, g, a)], buf=dense_pw[(K, N, g, a)].buf.clone())
+                for _ in range(max(1, -(-2 * L2_BYTES // (K * N // 2))) )]
     weight_copies_bytes = sum(wbytes(*lk) * len(packed[lk]) for lk in layers)
     max_m = max(p.M for p in problems)
     ws = {lk: w4.Workspace(max_m, lk[0], lk[1], lk[2]) for lk in layers}
@@ -349,7 +381,7 @@ def run_gpu(args, problems, rank, world, local):
         for i, c in plan:
             p = problems[i]
             lk = (p.K, p.N, p.group, p.asym)
-            w4.gemm_into(xs[i], packed[lk][c], ws[lk], ys[i])
+            call(xs[i], packed[lk][c], ws[lk], ys[i])
 
     # eager warm-up (one-time host set-up happens outside the graphs)
     for plan in plans:
@@ -411,10 +443,10 @@ def run_gpu(args, problems, rank, world, local):
     # ---- per-run table (outside the timed region): our kernel vs cuBLAS fp16 ----
     runs = []
     if not args.no_table:
-        runs = per_run_table(problems, packed, ws, xs, ys, dev, peaks)
+        runs = per_run_table(problems, packed, ws, xs, ys, dev, peaks, call, dense_pw if sparse else None)
 
     # ---- end to end through the public API with host buffers ----
-    e2e = None if args.no_e2e else end_to_end(problems, packed, ws, plans, dev, args, step_bytes)
+    e2e = None if args.no_e2e else end_to_end(problems, packed, ws, plans, dev, args, step_bytes, call)
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -458,7 +490,10 @@ def run_gpu(args, problems, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
-def per_run_table(problems, packed, ws, xs, ys, dev, peaks):
+def per_run_table(problems, packed, ws, xs, ys, dev, peaks, call, dense_packed=None):
+    """Per problem: our call vs cuBLAS fp16 (and, for 2:4 weights, vs the dense
+    kernel on the same weights in the dense layout), each timed as a CUDA graph
+    of repeated launches over rotating weight copies."""
     import torch
 
     import w4a16_mixed_precision_gb300 as w4
@@ -483,18 +518,26 @@ def per_run_table(problems, packed, ws, xs, ys, dev, peaks):
         # copies, so host launch cost does not enter the per-call time
         with torch.cuda.stream(stream):
             for _ in range(3):
-                w4.gemm_into(xs[i], packed[lk][0], ws[lk], ys[i])
+                call(xs[i], packed[lk][0], ws[lk], ys[i])
                 torch.matmul(xs[i], fp16_w[lk][0])
             stream.synchronize()
             g_ours, g_ref = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
             with torch.cuda.graph(g_ours, stream=stream):
                 for r in range(reps):
-                    w4.gemm_into(xs[i], packed[lk][r % R], ws[lk], ys[i])
+                    call(xs[i], packed[lk][r % R], ws[lk], ys[i])
             with torch.cuda.graph(g_ref, stream=stream):
                 for r in range(reps):
                     torch.matmul(xs[i], fp16_w[lk][r % Rf])
+            graphs = [g_ours, g_ref]
+            if dense_packed is not None:
+                dc = dense_packed[lk]
+                g_dense = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g_dense, stream=stream):
+                    for r in range(reps):
+                        w4.gemm_into(xs[i], dc[r % len(dc)], ws[lk], ys[i])
+                graphs.append(g_dense)
             times = []
-            for g in (g_ours, g_ref):
+            for g in graphs:
                 g.replay()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
@@ -502,18 +545,22 @@ def per_run_table(problems, packed, ws, xs, ys, dev, peaks):
                 e1.record(stream)
                 stream.synchronize()
                 times.append(e0.elapsed_time(e1) * 1e3 / reps)
-        us, cu = times
+        us, cu = times[0], times[1]
         gbs = p.algorithmic_bytes() / (us * 1e-6) / 1e9
         tfl = p.flops() / (us * 1e-6) / 1e12
-        out.append({"M": p.M, "K": p.K, "N": p.N, "group": p.group, "zeros": p.asym, "us": round(us, 3),
-                    "GBps": round(gbs, 1), "TFLOPs": round(tfl, 2),
-                    "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
-                    "tensor_frac": round(tfl / peaks["bf16_tflops"], 4),
-                    "cublas_fp16_us": round(cu, 3), "speedup_vs_fp16": round(cu / us, 3)})
+        row = {"M": p.M, "K": p.K, "N": p.N, "group": p.group, "zeros": p.asym, "us": round(us, 3),
+               "GBps": round(gbs, 1), "TFLOPs": round(tfl, 2),
+               "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+               "tensor_frac": round(tfl / peaks["bf16_tflops"], 4),
+               "cublas_fp16_us": round(cu, 3), "speedup_vs_fp16": round(cu / us, 3)}
+        if dense_packed is not None:
+            row["dense_kernel_us"] = round(times[2], 3)
+            row["speedup_vs_dense"] = round(times[2] / us, 3)
+        out.append(row)
     return out
 
 
-def end_to_end(problems, packed, ws, plans, dev, args, step_bytes):
+def end_to_end(problems, packed, ws, plans, dev, args, step_bytes, call):
     """The step through the public API with host buffers: every step copies all
     of its activations in from pinned host memory (one copy of one buffer that
     holds every problem's X), makes the 24 marlin_gemm calls (gemm_into), and
@@ -548,7 +595,7 @@ def end_to_end(problems, packed, ws, plans, dev, args, step_bytes):
         for i, c in plan:
             p = problems[i]
             lk = (p.K, p.N, p.group, p.asym)
-            w4.gemm_into(dx[i], packed[lk][c], ws[lk], dy[i])
+            call(dx[i], packed[lk][c], ws[lk], dy[i])
         hy.copy_(dyb, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
@@ -570,7 +617,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="7b-decode", choices=sorted(ALL_CONFIGS))
+    ap.add_argument("--workload", default="7b-decode", choices=sorted(ALL_CONFIGS) + sorted(SPARSE_CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-table", action="store_true", help="skip the per-run table")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -581,7 +628,7 @@ def main():
                     help="one problem M,K,N[,group[,asym]] instead of a workload (profiling a single kernel)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
-    problems = ALL_CONFIGS[args.workload]
+    problems = {**ALL_CONFIGS, **SPARSE_CONFIGS}[args.workload]
     if args.shape:
         v = [int(t) for t in args.shape.split(",")]
         M, K, N = v[0], v[1], v[2]

@@ -215,6 +215,84 @@ marlin_status_t marlin_gemm_host(const uint16_t* X_host, uint16_t* X_dev, const 
                                  void* workspace, size_t workspace_bytes, marlin_stream_t stream);
 
 /*
+ * ---- 2:4-sparse variant ----------------------------------------------------
+ *
+ * "Marlin" (dingiv.github.io), section "支持 2:4 稀疏加速": the weights are
+ * pruned ahead of time so that two of every four are zero, at fixed
+ * positions; "Marlin / GPTQ-Marlin" (brain.gartu.xyz), section "4. Support de
+ * la sparsité 2:4 NVIDIA": after dequantisation the zeros are skipped and the
+ * sparse tensor core multiplies only the kept half.
+ *
+ * This library's reading: a weight is zero exactly when its code equals its
+ * zero point (dequant = (q - z) * s), and the four weights of a group are four
+ * consecutive rows k = 4j .. 4j+3 of one column (along K, the direction the
+ * sparse tensor core compresses).  Inputs are the dense formats above (q,
+ * scales, zeros); the product is the same Y = X . dequant(W) as marlin_gemm's.
+ * In each group the kept rows are those whose code differs from z, in
+ * ascending order, completed with the lowest remaining rows.
+ */
+
+/*
+ * Size and offsets of the repacked 2:4 buffer, laid out as
+ * [codes | meta | scales | zeros]:
+ *   codes  K*N/4 bytes: the two kept codes of every group (tile layout below);
+ *   meta   K*N/8 bytes at *off_meta: a 4-bit index pair i0 | i1 << 2 per group;
+ *   scales, zeros as in marlin_packed_layout, at *off_scales / *off_zeros.
+ * All offsets are multiples of 256 bytes.  Host-only, no CUDA call; each
+ * output pointer may be NULL.  Errors: INVALID_ARG (shape/group).
+ */
+marlin_status_t marlin_sparse_packed_layout(int K, int N, int group, int has_zeros, size_t* bytes,
+                                            size_t* off_meta, size_t* off_scales, size_t* off_zeros);
+
+/*
+ * Offline repack of 2:4-sparse weights into the sparse tile layout.
+ *
+ * q, scales, zeros  device, the dense input formats (read only); zeros NULL
+ *                   means z = 8.
+ * out               device, marlin_sparse_packed_layout(...) bytes, 16-byte
+ *                   aligned, written; must not overlap the inputs.
+ * bad_groups        device int or NULL.  The repack adds to it (atomically)
+ *                   the number of groups of four rows in which more than two
+ *                   codes differ from z, i.e. where the weights are not 2:4;
+ *                   such a group keeps its first two non-zero rows and the
+ *                   product no longer equals the dense one.  Zero it before
+ *                   the call and check it after the stream is synchronised.
+ * Layout of `out` (the operand order of the 16 x 32 sparse fp16 tensor-core
+ * fragment), per 128-column tile nt < N/128 and 64-row chunk kb < K/64:
+ *   codes  32-bit word ((nt*(K/64) + kb)*8 + gq)*64 + l*2 + s (gq < 8, l < 32,
+ *          s < 2) holds at bits 4p..4p+3 the kept code number p >> 2 of
+ *          column n = nt*128 + 16gq + l/4 + 8*(p & 1) in group
+ *          j = kb*16 + 8s + l%4 + 4*((p >> 1) & 1) (rows 4j .. 4j+3);
+ *   meta   word ((nt*(K/64) + kb)*8 + gq)*32 + (r*2 + h)*2 + s (r < 8, h < 2,
+ *          s < 2) at off_meta holds at bits 4i..4i+3 the index pair of column
+ *          n = nt*128 + 16gq + r + 8*(i >> 2) in group j = kb*16 + 8s + 4h + (i & 3);
+ *   scales, zeros as for marlin_repack.
+ * Errors: INVALID_ARG (shape/group/NULL), MISALIGNED (16-byte buffers,
+ * 4-byte bad_groups), CUDA (launch).
+ */
+marlin_status_t marlin_sparse_repack(const int32_t* q, const uint16_t* scales, const int32_t* zeros,
+                                     int K, int N, int group, void* out, int* bad_groups,
+                                     marlin_stream_t stream);
+
+/*
+ * Y = X . dequant(W) for 2:4-sparse weights: dequantises only the kept half
+ * of the codes and multiplies with mma.sp on the warp-level path (M <= 32).
+ *
+ * packed     device, the codes region of a marlin_sparse_repack output.
+ * meta       device, the meta region (packed + off_meta); NULL -> INVALID_ARG.
+ * scales     device, packed + off_scales.  zeros: packed + off_zeros or NULL.
+ * X, Y, workspace, stream, determinism, errors: as for marlin_gemm; a
+ * workspace sized by marlin_workspace_bytes(M, K, N, group, ...) serves this
+ * call too.  M > 32 -> MARLIN_ERR_UNSUPPORTED.  Results agree with
+ * marlin_gemm's on the expanded weights within the parity tolerance (the
+ * fp32 summation orders differ).
+ */
+marlin_status_t marlin_sparse_gemm(const uint16_t* X, const void* packed, const void* meta,
+                                   const uint16_t* scales, const int32_t* zeros, uint16_t* Y, int M,
+                                   int K, int N, int group, void* workspace, size_t workspace_bytes,
+                                   marlin_stream_t stream);
+
+/*
  * Synchronises `stream`, reads and clears the device status word that
  * marlin_gemm keeps in `workspace`, and returns MARLIN_OK or
  * MARLIN_ERR_TIMEOUT (a bounded wait in a kernel expired; that call's Y is

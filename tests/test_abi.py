@@ -95,3 +95,38 @@ def test_product_path_does_not_import_the_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in src and "from oracle" not in src, f
                 assert "oracle.c" not in src, f
+
+
+def test_sparse_packed_layout(lib):
+    from w4a16_mixed_precision_gb300 import _binding
+    b, m, s, z = _binding.sparse_packed_layout(4096, 4096, 128, False)
+    assert m == 4096 * 4096 // 4                       # kept codes: half of the dense codes
+    assert s == m + 4096 * 4096 // 8                   # index pairs: 4 bits per four weights
+    assert b == s + 32 * 4096 * 2 and z == b
+    b, m, s, z = _binding.sparse_packed_layout(2048, 5632, -1, True)
+    assert m % 256 == 0 and s % 256 == 0 and z % 256 == 0
+    assert m >= 2048 * 5632 // 4 and s >= m + 2048 * 5632 // 8
+    assert z == s + 5632 * 2 and b == z + 5632 // 2
+    for bad in [(100, 128, 128), (256, 128, 64), (0, 128, 128)]:
+        with pytest.raises(_binding.MarlinError) as e:
+            _binding.sparse_packed_layout(*bad, False)
+        assert e.value.status == _binding.ERR_INVALID_ARG
+
+
+def test_sparse_host_checks(lib):
+    """The 2:4 entry points reject bad arguments before touching CUDA."""
+    from w4a16_mixed_precision_gb300 import _binding as b
+    g = 0x10000
+    call = b.sparse_gemm_raw
+    # meta is required; M > 32 is not served (warp-level path only)
+    assert call(g, g, None, g, None, g, 4, 256, 256, 128, g, 1 << 20, 0) == b.ERR_INVALID_ARG
+    assert call(g, g, g, g, None, g, 33, 256, 256, 128, g, 1 << 20, 0) == b.ERR_UNSUPPORTED
+    assert call(g, g, g, g, None, g, 0, 256, 256, 128, g, 1 << 20, 0) == b.OK
+    assert call(g, g, g, g, None, g, 4, 256, 200, 128, g, 1 << 20, 0) == b.ERR_INVALID_ARG
+    assert call(g, g, g + 8, g, None, g, 4, 256, 256, 128, g, 1 << 20, 0) == b.ERR_MISALIGNED
+    assert call(g, g + 8, g, g, None, g, 4, 256, 256, 128, g, 1 << 20, 0) == b.ERR_MISALIGNED
+    rp = b.sparse_repack_raw
+    assert rp(0, g, None, 256, 256, 128, g, None, 0) == b.ERR_INVALID_ARG
+    assert rp(g, g, None, 256, 256, 96, g, None, 0) == b.ERR_INVALID_ARG
+    assert rp(g, g, None, 256, 256, 128, g + 8, None, 0) == b.ERR_MISALIGNED
+    assert rp(g, g, None, 256, 256, 128, g, g + 2, 0) == b.ERR_MISALIGNED

@@ -21,7 +21,8 @@ from . import _binding
 from ._binding import MarlinError, status_string  # noqa: F401
 
 __all__ = ["PackedWeights", "Workspace", "repack", "gemm", "gemm_into", "gemm_host", "device_status",
-           "MarlinError", "status_string", "packed_layout"]
+           "MarlinError", "status_string", "packed_layout", "SparsePackedWeights", "sparse_repack",
+           "sparse_gemm", "sparse_gemm_into"]
 
 
 def _stream() -> int:
@@ -153,3 +154,80 @@ def gemm_host(x_host: torch.Tensor, x_dev: torch.Tensor, w: PackedWeights, ws: W
 def device_status(ws: Workspace) -> int:
     """Synchronise the current stream and read/clear the kernel status word."""
     return _binding.last_device_status(ws.ptr, _stream())
+
+
+# ---- 2:4-sparse variant ----------------------------------------------------------
+
+@dataclass
+class SparsePackedWeights:
+    """A repacked 2:4-sparse K x N weight: one uint8 buffer [codes | meta | scales | zeros]."""
+    buf: torch.Tensor
+    K: int
+    N: int
+    group: int
+    has_zeros: bool
+    off_meta: int
+    off_scales: int
+    off_zeros: int
+    bad_groups: int  # groups of four rows with more than two non-zero weights (0 for 2:4 weights)
+
+    @property
+    def codes_ptr(self) -> int:
+        return self.buf.data_ptr()
+
+    @property
+    def meta_ptr(self) -> int:
+        return self.buf.data_ptr() + self.off_meta
+
+    @property
+    def scales_ptr(self) -> int:
+        return self.buf.data_ptr() + self.off_scales
+
+    @property
+    def zeros_ptr(self) -> int | None:
+        return self.buf.data_ptr() + self.off_zeros if self.has_zeros else None
+
+
+def sparse_repack(q: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor | None, group: int,
+                  strict: bool = True) -> SparsePackedWeights:
+    """2:4-sparse GPTQ-order codes (same input formats as repack) ->
+    SparsePackedWeights (marlin_sparse_repack).  Synchronises the current
+    stream to read the count of groups that are not 2:4; strict: raise if any."""
+    _need_cuda(q, "q", torch.int32)
+    _need_cuda(scales, "scales", torch.float16)
+    if zeros is not None:
+        _need_cuda(zeros, "zeros", torch.int32)
+    K, N = q.shape[0] * 8, q.shape[1]
+    g = K if group == -1 else group
+    nbytes, off_m, off_s, off_z = _binding.sparse_packed_layout(K, N, g, zeros is not None)
+    out = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    bad = torch.zeros(1, dtype=torch.int32, device=q.device)
+    rc = _binding.sparse_repack_raw(q.data_ptr(), scales.data_ptr(),
+                                    zeros.data_ptr() if zeros is not None else None, K, N, g,
+                                    out.data_ptr(), bad.data_ptr(), _stream())
+    if rc != _binding.OK:
+        raise MarlinError(rc, "marlin_sparse_repack")
+    nbad = int(bad.item())
+    if strict and nbad:
+        raise ValueError(f"weights are not 2:4 sparse: {nbad} groups of four rows have more than "
+                         "two codes that differ from the zero point")
+    return SparsePackedWeights(out, K, N, g, zeros is not None, off_m, off_s, off_z, nbad)
+
+
+def sparse_gemm_into(x: torch.Tensor, w: SparsePackedWeights, ws: Workspace, y: torch.Tensor) -> torch.Tensor:
+    """y[M, N] = x[M, K] . dequant(W) for 2:4-sparse W (M <= 32), fp16, on the current stream."""
+    _need_cuda(x, "x", torch.float16)
+    _need_cuda(y, "y", torch.float16)
+    M, K = x.shape
+    if K != w.K or tuple(y.shape) != (M, w.N):
+        raise ValueError("shape mismatch")
+    rc = _binding.sparse_gemm_raw(x.data_ptr(), w.codes_ptr, w.meta_ptr, w.scales_ptr, w.zeros_ptr,
+                                  y.data_ptr(), M, K, w.N, w.group, ws.ptr, ws.nbytes, _stream())
+    if rc != _binding.OK:
+        raise MarlinError(rc, "marlin_sparse_gemm")
+    return y
+
+
+def sparse_gemm(x: torch.Tensor, w: SparsePackedWeights, ws: Workspace) -> torch.Tensor:
+    y = torch.empty((x.shape[0], w.N), dtype=torch.float16, device=x.device)
+    return sparse_gemm_into(x, w, ws, y)

@@ -33,6 +33,9 @@ EXPORTS = (
     "marlin_gemm_no_alloc",
     "marlin_gemm_host",
     "marlin_last_device_status",
+    "marlin_sparse_packed_layout",
+    "marlin_sparse_repack",
+    "marlin_sparse_gemm",
 )
 
 
@@ -72,6 +75,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.marlin_gemm_no_alloc.restype = I
         lib.marlin_gemm_host.argtypes = [P, P, P, P, P, P, P, I, I, I, I, P, SZ, P]
         lib.marlin_gemm_host.restype = I
+        lib.marlin_sparse_packed_layout.argtypes = [I, I, I, I] + [ctypes.POINTER(SZ)] * 4
+        lib.marlin_sparse_repack.argtypes = [P, P, P, I, I, I, P, P, P]
+        lib.marlin_sparse_gemm.argtypes = [P, P, P, P, P, P, I, I, I, I, P, SZ, P]
+        for f in ("marlin_sparse_packed_layout", "marlin_sparse_repack", "marlin_sparse_gemm"):
+            getattr(lib, f).restype = I
         for f in ("marlin_packed_layout", "marlin_repack", "marlin_workspace_bytes", "marlin_gemm",
                   "marlin_last_device_status"):
             getattr(lib, f).restype = I
@@ -145,3 +153,27 @@ def gemm_no_alloc_raw(x_ptr: int, packed_ptr: int, scales_ptr: int, zeros_ptr: i
 
 def last_device_status(ws_ptr: int, stream: int) -> int:
     return load().marlin_last_device_status(ws_ptr, stream or None)
+
+
+def sparse_packed_layout(K: int, N: int, group: int, has_zeros: bool):
+    """(bytes, off_meta, off_scales, off_zeros) of the repacked 2:4 buffer."""
+    b, m, sc, z = (ctypes.c_size_t() for _ in range(4))
+    _check(load().marlin_sparse_packed_layout(K, N, group, int(bool(has_zeros)), ctypes.byref(b),
+                                              ctypes.byref(m), ctypes.byref(sc), ctypes.byref(z)),
+           "marlin_sparse_packed_layout")
+    return b.value, m.value, sc.value, z.value
+
+
+def sparse_repack_raw(q_ptr: int, scales_ptr: int, zeros_ptr: int | None, K: int, N: int, group: int,
+                      out_ptr: int, bad_ptr: int | None, stream: int) -> int:
+    """Raw call of the 2:4 repack; returns the status code."""
+    return load().marlin_sparse_repack(q_ptr, scales_ptr, zeros_ptr or None, K, N, group, out_ptr,
+                                       bad_ptr or None, stream or None)
+
+
+def sparse_gemm_raw(x_ptr: int, packed_ptr: int, meta_ptr: int | None, scales_ptr: int,
+                    zeros_ptr: int | None, y_ptr: int, M: int, K: int, N: int, group: int, ws_ptr: int,
+                    ws_bytes: int, stream: int) -> int:
+    """Raw call of the 2:4-sparse multiply; returns the status code."""
+    return load().marlin_sparse_gemm(x_ptr, packed_ptr, meta_ptr or None, scales_ptr, zeros_ptr or None,
+                                     y_ptr, M, K, N, group, ws_ptr, ws_bytes, stream or None)

@@ -102,8 +102,10 @@ int xmap_slot(const void* X, int M, int K, int bn) {
 // cpu*64 rows); the grid is one CTA per SM (fewer if there are fewer units),
 // each taking an equal contiguous stripe of units.
 // kernel: MARLIN_KERNEL_AUTO picks by M (small_m_max); the others force one.
+// sparse: 2:4 weights (the warp-level kernel; stages carry the kept codes and
+// their index nibbles instead of the dense codes).
 GemmPlan make_plan(int M, int K, int N, int group, int sms, int smem_optin, bool has_zeros,
-                   int kernel = MARLIN_KERNEL_AUTO) {
+                   int kernel = MARLIN_KERNEL_AUTO, bool sparse = false) {
   GemmPlan g{};
   g.n_tiles = N / kTileN;
   const int budget = smem_optin - kCtrlBytes - 1024;  // control block + alignment slack
@@ -142,7 +144,8 @@ GemmPlan make_plan(int M, int K, int N, int group, int sms, int smem_optin, bool
   g.units = (long long)g.m_tiles * g.n_tiles * g.kt;
   g.grid = (int)(g.units < sms ? g.units : sms);
   const size_t x_chunk = (size_t)g.bn * 128;
-  const size_t stage = g.cpu * (x_chunk + kChunkCodeBytes) +
+  const size_t chunk_w = sparse ? (size_t)(kSpChunkCodeBytes + kSpChunkMetaBytes) : kChunkCodeBytes;
+  const size_t stage = g.cpu * (x_chunk + chunk_w) +
                        (size_t)g.n_g * (kTileN * 2 + (has_zeros ? kTileN / 2 : 0));
   g.stage_bytes = (uint32_t)round_up(stage, 1024);
   const size_t xchg = g.kind == kKernelSmallM ? (size_t)4 * (g.bn / 8) * 256 * sizeof(float) : 0;
@@ -167,6 +170,114 @@ GemmPlan make_plan(int M, int K, int N, int group, int sms, int smem_optin, bool
 
 marlin_status_t current_device(int* dev) {
   return cudaGetDevice(dev) == cudaSuccess ? MARLIN_OK : MARLIN_ERR_CUDA;
+}
+
+// The checks, the plan and the launch shared by marlin_gemm_ex and
+// marlin_sparse_gemm.  meta != nullptr: the 2:4-sparse variant (packed and
+// meta in the sparse tile layout; warp-level kernel only).
+marlin_status_t run_gemm(const uint16_t* X, const void* packed, const void* meta,
+                         const uint16_t* scales, const int32_t* zeros, uint16_t* Y, int M, int K,
+                         int N, int group, void* workspace, size_t workspace_bytes, int kernel,
+                         marlin_stream_t stream) {
+  const bool sparse = meta != nullptr;
+  if (M < 0 || !valid_shape(K, N) || !normalise_group(K, &group)) return MARLIN_ERR_INVALID_ARG;
+  if (sparse) kernel = MARLIN_KERNEL_WARP;
+  if (kernel == MARLIN_KERNEL_WARP && M > kMaxWarpM) return MARLIN_ERR_UNSUPPORTED;
+  if (M == 0) return MARLIN_OK;
+  if (!X || !packed || !scales || !Y || !workspace) return MARLIN_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(packed) || !aligned16(scales) || (zeros && !aligned16(zeros)) ||
+      (meta && !aligned16(meta)) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(Y) & 1u))
+    return MARLIN_ERR_MISALIGNED;
+  int dev;
+  marlin_status_t s = current_device(&dev);
+  if (s != MARLIN_OK) return s;
+  DeviceState* d;
+  if ((s = device_state(dev, &d)) != MARLIN_OK) return s;
+  if ((s = get_encoder()) != MARLIN_OK) return s;
+
+  const GemmPlan g = make_plan(M, K, N, group, d->sms, d->smem_optin, zeros != nullptr, kernel, sparse);
+  if (g.stages < 2 || g.units > 0x7FFFFFFFLL / 2) return MARLIN_ERR_UNSUPPORTED;
+  if (g.kind == kKernelTcgen05 && g.a_slots < 4) return MARLIN_ERR_UNSUPPORTED;
+  if (workspace_bytes < g.ws_bytes) return MARLIN_ERR_WORKSPACE_TOO_SMALL;
+
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!d->smem_set) {
+      if (gemm_set_smem_limit(d->smem_optin) != cudaSuccess ||
+          small_m_set_smem_limit(d->smem_optin) != cudaSuccess)
+        return MARLIN_ERR_CUDA;
+      d->smem_set = true;
+    }
+  }
+
+  // X's tensor map depends only on (address, M, K, box rows): keep the last
+  // few per host thread, so a decode loop over fixed buffers encodes each once
+  XMapEntry& xe = t_xmaps[xmap_slot(X, M, K, g.bn)];
+  if (!(xe.valid && xe.X == X && xe.M == M && xe.K == K && xe.bn == g.bn)) {
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kChunkK, (cuuint32_t)g.bn};
+    const cuuint32_t estr[2] = {1, 1};
+    xe.valid = false;
+    if (g_encode(&xe.map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(X), dims, strides,
+                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MARLIN_ERR_CUDA;
+    xe.X = X;
+    xe.M = M;
+    xe.K = K;
+    xe.bn = g.bn;
+    xe.valid = true;
+  }
+  const CUtensorMap& x_map = xe.map;
+
+  GemmParams p{};
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.codes = static_cast<const uint32_t*>(packed);
+  p.meta = static_cast<const uint32_t*>(meta);
+  p.scales = scales;
+  p.zeros = reinterpret_cast<const uint8_t*>(zeros);
+  p.Y = Y;
+  p.status = reinterpret_cast<int*>(ws);
+  p.counters = reinterpret_cast<int*>(ws + g.ws_counters_off);
+  p.partials = reinterpret_cast<float*>(ws + g.ws_partials_off);
+  p.M = M;
+  p.K = K;
+  p.N = N;
+  p.group = group;
+  p.G = K / group;
+  p.bn = g.bn;
+  p.m_tiles = g.m_tiles;
+  p.n_tiles = g.n_tiles;
+  p.kt = g.kt;
+  p.cpu = g.cpu;
+  p.units = g.units;
+  p.stages = g.stages;
+  p.stage_bytes = g.stage_bytes;
+  p.x_chunk_bytes = (uint32_t)g.bn * 128;
+  p.off_codes = (uint32_t)g.cpu * p.x_chunk_bytes;
+  p.off_meta = p.off_codes + (uint32_t)g.cpu * (sparse ? kSpChunkCodeBytes : kChunkCodeBytes);
+  p.off_scales = sparse ? p.off_meta + (uint32_t)g.cpu * kSpChunkMetaBytes : p.off_meta;
+  p.off_zeros = p.off_scales + (uint32_t)g.n_g * kTileN * 2;
+  p.weights_reused = g.m_tiles > 1;
+  p.nacc = g.nacc > 0 ? g.nacc : 1;
+  p.split_n = g.split_n;
+  p.split_h = g.bn > 128 ? 128 : (int)round_up((size_t)(g.bn / 2), 16);
+  p.full_all = (g.stages % 4) != 0;
+  p.a_slots = g.a_slots;
+  p.a_base = (uint32_t)(kTmemCols - g.a_slots * g.cpu * (kChunkK / 2));
+  p.tx_w = (uint32_t)g.cpu * kChunkCodeBytes + (uint32_t)g.n_g * (kTileN * 2 + (zeros ? kTileN / 2 : 0));
+  p.tx_x = (uint32_t)g.cpu * p.x_chunk_bytes;
+  p.n_g = g.n_g;
+  p.units_per_group = g.upg;
+  p.off_xchg = g.off_xchg;
+  p.timeout_ns = kDefaultTimeoutNs;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t e = g.kind == kKernelSmallM
+                            ? launch_small_m(x_map, p, g.grid, g.smem_bytes, sparse, st)
+                            : launch_gemm(x_map, p, g.grid, g.smem_bytes, st);
+  if (e != cudaSuccess) return MARLIN_ERR_CUDA;
+  return MARLIN_OK;
 }
 
 }  // namespace
@@ -249,102 +360,10 @@ marlin_status_t marlin_gemm_ex(const uint16_t* X, const void* packed, const uint
                                const int32_t* zeros, uint16_t* Y, int M, int K, int N, int group,
                                void* workspace, size_t workspace_bytes, marlin_kernel_t kernel,
                                marlin_stream_t stream) {
-  if (M < 0 || !valid_shape(K, N) || !normalise_group(K, &group)) return MARLIN_ERR_INVALID_ARG;
   if (kernel != MARLIN_KERNEL_AUTO && kernel != MARLIN_KERNEL_WARP && kernel != MARLIN_KERNEL_TCGEN05)
     return MARLIN_ERR_INVALID_ARG;
-  if (kernel == MARLIN_KERNEL_WARP && M > kMaxWarpM) return MARLIN_ERR_UNSUPPORTED;
-  if (M == 0) return MARLIN_OK;
-  if (!X || !packed || !scales || !Y || !workspace) return MARLIN_ERR_INVALID_ARG;
-  if (!aligned16(X) || !aligned16(packed) || !aligned16(scales) || (zeros && !aligned16(zeros)) ||
-      !aligned16(workspace) || (reinterpret_cast<uintptr_t>(Y) & 1u))
-    return MARLIN_ERR_MISALIGNED;
-  int dev;
-  marlin_status_t s = current_device(&dev);
-  if (s != MARLIN_OK) return s;
-  DeviceState* d;
-  if ((s = device_state(dev, &d)) != MARLIN_OK) return s;
-  if ((s = get_encoder()) != MARLIN_OK) return s;
-
-  const GemmPlan g = make_plan(M, K, N, group, d->sms, d->smem_optin, zeros != nullptr, kernel);
-  if (g.stages < 2 || g.units > 0x7FFFFFFFLL / 2) return MARLIN_ERR_UNSUPPORTED;
-  if (g.kind == kKernelTcgen05 && g.a_slots < 4) return MARLIN_ERR_UNSUPPORTED;
-  if (workspace_bytes < g.ws_bytes) return MARLIN_ERR_WORKSPACE_TOO_SMALL;
-
-  {
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (!d->smem_set) {
-      if (gemm_set_smem_limit(d->smem_optin) != cudaSuccess ||
-          small_m_set_smem_limit(d->smem_optin) != cudaSuccess)
-        return MARLIN_ERR_CUDA;
-      d->smem_set = true;
-    }
-  }
-
-  // X's tensor map depends only on (address, M, K, box rows): keep the last
-  // few per host thread, so a decode loop over fixed buffers encodes each once
-  XMapEntry& xe = t_xmaps[xmap_slot(X, M, K, g.bn)];
-  if (!(xe.valid && xe.X == X && xe.M == M && xe.K == K && xe.bn == g.bn)) {
-    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kChunkK, (cuuint32_t)g.bn};
-    const cuuint32_t estr[2] = {1, 1};
-    xe.valid = false;
-    if (g_encode(&xe.map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(X), dims, strides,
-                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return MARLIN_ERR_CUDA;
-    xe.X = X;
-    xe.M = M;
-    xe.K = K;
-    xe.bn = g.bn;
-    xe.valid = true;
-  }
-  const CUtensorMap& x_map = xe.map;
-
-  GemmParams p{};
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  p.codes = static_cast<const uint32_t*>(packed);
-  p.scales = scales;
-  p.zeros = reinterpret_cast<const uint8_t*>(zeros);
-  p.Y = Y;
-  p.status = reinterpret_cast<int*>(ws);
-  p.counters = reinterpret_cast<int*>(ws + g.ws_counters_off);
-  p.partials = reinterpret_cast<float*>(ws + g.ws_partials_off);
-  p.M = M;
-  p.K = K;
-  p.N = N;
-  p.group = group;
-  p.G = K / group;
-  p.bn = g.bn;
-  p.m_tiles = g.m_tiles;
-  p.n_tiles = g.n_tiles;
-  p.kt = g.kt;
-  p.cpu = g.cpu;
-  p.units = g.units;
-  p.stages = g.stages;
-  p.stage_bytes = g.stage_bytes;
-  p.x_chunk_bytes = (uint32_t)g.bn * 128;
-  p.off_codes = (uint32_t)g.cpu * p.x_chunk_bytes;
-  p.off_scales = p.off_codes + (uint32_t)g.cpu * kChunkCodeBytes;
-  p.off_zeros = p.off_scales + (uint32_t)g.n_g * kTileN * 2;
-  p.weights_reused = g.m_tiles > 1;
-  p.nacc = g.nacc > 0 ? g.nacc : 1;
-  p.split_n = g.split_n;
-  p.split_h = g.bn > 128 ? 128 : (int)round_up((size_t)(g.bn / 2), 16);
-  p.full_all = (g.stages % 4) != 0;
-  p.a_slots = g.a_slots;
-  p.a_base = (uint32_t)(kTmemCols - g.a_slots * g.cpu * (kChunkK / 2));
-  p.tx_w = (uint32_t)g.cpu * kChunkCodeBytes + (uint32_t)g.n_g * (kTileN * 2 + (zeros ? kTileN / 2 : 0));
-  p.tx_x = (uint32_t)g.cpu * p.x_chunk_bytes;
-  p.n_g = g.n_g;
-  p.units_per_group = g.upg;
-  p.off_xchg = g.off_xchg;
-  p.timeout_ns = kDefaultTimeoutNs;
-  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const cudaError_t e = g.kind == kKernelSmallM ? launch_small_m(x_map, p, g.grid, g.smem_bytes, st)
-                                                : launch_gemm(x_map, p, g.grid, g.smem_bytes, st);
-  if (e != cudaSuccess) return MARLIN_ERR_CUDA;
-  return MARLIN_OK;
+  return run_gemm(X, packed, nullptr, scales, zeros, Y, M, K, N, group, workspace, workspace_bytes,
+                  kernel, stream);
 }
 
 marlin_status_t marlin_gemm_host(const uint16_t* X_host, uint16_t* X_dev, const void* packed,
@@ -376,6 +395,57 @@ marlin_status_t marlin_gemm_host(const uint16_t* X_host, uint16_t* X_dev, const 
   if (cudaMemcpyAsync(Y_host, Y_dev, (size_t)M * N * 2, cudaMemcpyDeviceToHost, st) != cudaSuccess)
     return MARLIN_ERR_CUDA;
   return MARLIN_OK;
+}
+
+// ---- 2:4-sparse variant ----------------------------------------------------------
+
+marlin_status_t marlin_sparse_packed_layout(int K, int N, int group, int has_zeros, size_t* bytes,
+                                            size_t* off_meta, size_t* off_scales, size_t* off_zeros) {
+  if (!valid_shape(K, N) || !normalise_group(K, &group)) return MARLIN_ERR_INVALID_ARG;
+  const size_t G = (size_t)(K / group);
+  const size_t codes = (size_t)K * N / 4;
+  const size_t me = round_up(codes, 256);
+  const size_t sc = round_up(me + (size_t)K * N / 8, 256);
+  const size_t zo = round_up(sc + G * N * 2, 256);
+  const size_t total = has_zeros ? zo + G * N / 2 : zo;
+  if (bytes) *bytes = total;
+  if (off_meta) *off_meta = me;
+  if (off_scales) *off_scales = sc;
+  if (off_zeros) *off_zeros = has_zeros ? zo : total;
+  return MARLIN_OK;
+}
+
+marlin_status_t marlin_sparse_repack(const int32_t* q, const uint16_t* scales, const int32_t* zeros,
+                                     int K, int N, int group, void* out, int* bad_groups,
+                                     marlin_stream_t stream) {
+  if (!q || !scales || !out) return MARLIN_ERR_INVALID_ARG;
+  if (!valid_shape(K, N) || !normalise_group(K, &group)) return MARLIN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(scales) || !aligned16(out) || (zeros && !aligned16(zeros)) ||
+      (reinterpret_cast<uintptr_t>(bad_groups) & 3u))
+    return MARLIN_ERR_MISALIGNED;
+  size_t bytes, off_m, off_s, off_z;
+  marlin_sparse_packed_layout(K, N, group, zeros != nullptr, &bytes, &off_m, &off_s, &off_z);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* o = static_cast<uint8_t*>(out);
+  const size_t G = (size_t)(K / group);
+  if (launch_sparse_repack(reinterpret_cast<const uint32_t*>(q), reinterpret_cast<const uint32_t*>(zeros),
+                           K, N, group, reinterpret_cast<uint32_t*>(o),
+                           reinterpret_cast<uint32_t*>(o + off_m), bad_groups, st) != cudaSuccess)
+    return MARLIN_ERR_CUDA;
+  if (launch_tile_major(scales, o + off_s, (int)G, N, kTileN * 2, st) != cudaSuccess)
+    return MARLIN_ERR_CUDA;
+  if (zeros && launch_tile_major(zeros, o + off_z, (int)G, N, kTileN / 2, st) != cudaSuccess)
+    return MARLIN_ERR_CUDA;
+  return MARLIN_OK;
+}
+
+marlin_status_t marlin_sparse_gemm(const uint16_t* X, const void* packed, const void* meta,
+                                   const uint16_t* scales, const int32_t* zeros, uint16_t* Y, int M,
+                                   int K, int N, int group, void* workspace, size_t workspace_bytes,
+                                   marlin_stream_t stream) {
+  if (!meta) return MARLIN_ERR_INVALID_ARG;
+  return run_gemm(X, packed, meta, scales, zeros, Y, M, K, N, group, workspace, workspace_bytes,
+                  MARLIN_KERNEL_WARP, stream);
 }
 
 marlin_status_t marlin_last_device_status(void* workspace, marlin_stream_t stream) {

@@ -1,5 +1,5 @@
 // kernels.h -- internal interface between the C-ABI host layer (api.cu) and
-// the device kernels (gemm.cu, repack.cu).  Not installed, not part of the ABI.
+// the device kernels (gemm.cu, small_m.cu, repack.cu).  Not installed, not part of the ABI.
 #pragma once
 
 #include <cuda.h>
@@ -13,6 +13,10 @@ constexpr int kThreads = 640;      // 20 warps: 2 producers, 2 MMA issuers (one 
 constexpr int kTileN = 128;        // output columns per tile = UMMA M
 constexpr int kChunkK = 64;        // K elements per dequantised A chunk
 constexpr int kChunkCodeBytes = kTileN * kChunkK / 2;  // 4096
+// 2:4-sparse layout: per 64-row chunk of a tile, the kept half of the codes
+// and a 4-bit index pair per group of four rows
+constexpr int kSpChunkCodeBytes = kTileN * kChunkK / 4;  // 2048
+constexpr int kSpChunkMetaBytes = kTileN * kChunkK / 8;  // 1024
 constexpr int kMaxWarpM = 32;      // largest M the warp-level kernel serves (4 blocks of 8 tokens)
 constexpr int kAStages = 12;       // most A slots (one unit each) resident in TMEM
 constexpr int kTmemCols = 512;
@@ -25,6 +29,7 @@ constexpr int kStatusTimeout = 1;
 
 struct GemmParams {
   const uint32_t* codes;    // tile-layout codes
+  const uint32_t* meta;     // 2:4-sparse kernel: tile-layout index nibbles (else unused)
   const uint16_t* scales;   // fp16, tile-major [N/128][G][128]
   const uint8_t* zeros;     // zeros, tile-major bytes [N/128][G][64], or nullptr
   uint16_t* Y;              // fp16 [M][N]
@@ -41,6 +46,7 @@ struct GemmParams {
   uint32_t stage_bytes;
   uint32_t x_chunk_bytes;   // bn * 128
   uint32_t off_codes, off_scales, off_zeros;  // byte offsets inside a stage
+  uint32_t off_meta;        // 2:4-sparse kernel: index nibbles inside a stage
   int weights_reused;       // more than one m-tile reads the same weights
   int nacc;                 // tcgen05 kernel: MMA issuers, each with its own accumulator (1 or 2)
   int split_h;              // split_n: token columns of the first issuer (multiple of 16)
@@ -70,11 +76,17 @@ struct GemmPlan {
 cudaError_t launch_gemm(const CUtensorMap& x_map, const GemmParams& p, int grid, uint32_t smem_bytes,
                         cudaStream_t stream);
 cudaError_t gemm_set_smem_limit(int bytes);
+// sparse: the 2:4 variant (p.codes / p.meta in the sparse tile layout)
 cudaError_t launch_small_m(const CUtensorMap& x_map, const GemmParams& p, int grid,
-                           uint32_t smem_bytes, cudaStream_t stream);
+                           uint32_t smem_bytes, bool sparse, cudaStream_t stream);
 cudaError_t small_m_set_smem_limit(int bytes);
 
 cudaError_t launch_repack(const uint32_t* q, uint32_t* out, int K, int N, cudaStream_t stream);
+// 2:4: GPTQ-order codes (+ zeros) -> kept codes and index nibbles in the sparse
+// tile layout; *bad (if not null) += groups with more than two non-zero weights.
+cudaError_t launch_sparse_repack(const uint32_t* q, const uint32_t* zeros, int K, int N, int group,
+                                 uint32_t* codes_out, uint32_t* meta_out, int* bad,
+                                 cudaStream_t stream);
 // Rows of row_bytes (multiple of 16) from [G][N/128][row] to [N/128][G][row].
 cudaError_t launch_tile_major(const void* src, void* dst, int G, int N, int row_bytes,
                               cudaStream_t stream);

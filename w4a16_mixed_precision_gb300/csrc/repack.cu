@@ -1,5 +1,5 @@
 // repack.cu -- offline rewrite of GPTQ-order 4-bit codes, scales and zeros into
-// the layout the fused kernels stream ("Marlin / GPTQ-Marlin", section "Tiled
+// the layouts the fused kernels stream, dense and 2:4-sparse ("Marlin / GPTQ-Marlin", section "Tiled
 // layout et repacking": done once at load time; "Marlin Project Overview",
 // section "Key Techniques", item "Reshuffling for Access Patterns": weights and scales rearranged
 // offline into tensor-core operand order).
@@ -64,6 +64,110 @@ __global__ void tile_major_kernel(const uint4* __restrict__ src, uint4* __restri
   }
 }
 
+// ---- 2:4 sparsity ("Marlin", section "支持 2:4 稀疏加速": two of every four
+// weights zero at fixed positions) ----
+//
+// A weight is zero when its code equals the zero point.  In a group of four
+// consecutive rows of a column the kept rows are those whose code differs
+// from the zero point (the first two if there are more, which the caller is
+// told through *bad), completed with the lowest remaining rows; their index
+// pair i0 < i1 is the nibble i0 | i1 << 2, the metadata of a sparse
+// tensor-core operand.
+//
+// Sparse tile layout, per 128-column tile nt and 64-row chunk kb (16 groups):
+//   codes: word ((nt*KB + kb)*8 + gq)*64 + l*2 + s, nibble p: kept code
+//          (p >> 2) of column 16gq + l/4 + 8(p&1), group 8s + l%4 + 4((p>>1)&1);
+//   meta:  word ((nt*KB + kb)*8 + gq)*32 + (r*2 + h)*2 + s, nibble i: index pair
+//          of column 16gq + r + 8(i>>2), group 8s + 4h + (i&3).
+// So lane l = 4r + c of a warp holds, per 32-row step s, one code word whose
+// four fp16 pairs are its sparse A fragment registers, and lanes c = 0, 1 hold
+// the metadata words of the step's first and second 16 rows.
+
+// Codes of rows 4j..4j+3 of column n (nibble i = row 4j+i) and their zero point.
+__device__ __forceinline__ uint32_t group_codes(const uint32_t* q, int N, int j, int n) {
+  return (q[(size_t)(j >> 1) * N + n] >> ((j & 1) * 16)) & 0xFFFFu;
+}
+
+__device__ __forceinline__ uint32_t group_zero(const uint32_t* zeros, int N, int group, int j, int n) {
+  if (!zeros) return 8u;
+  return (zeros[(size_t)((4 * j) / group) * (N / 8) + n / 8] >> (4 * (n & 7))) & 0xFu;
+}
+
+// Kept-row mask of a group (two bits set) and whether it was 2:4.
+__device__ __forceinline__ uint32_t kept_mask(uint32_t codes4, uint32_t z, bool* ok) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m |= (((codes4 >> (4 * i)) & 0xFu) != z ? 1u : 0u) << i;
+  *ok = __popc(m) <= 2;
+  if (!*ok) {
+    const uint32_t lo = m & (0u - m);
+    const uint32_t rest = m ^ lo;
+    m = lo | (rest & (0u - rest));
+  }
+  while (__popc(m) < 2) m |= ~m & (m + 1u);  // lowest row not yet kept
+  return m;
+}
+
+__global__ void sparse_codes_kernel(const uint32_t* __restrict__ q, const uint32_t* __restrict__ zeros,
+                                    int K, int N, int group, uint32_t* __restrict__ out,
+                                    long long total) {
+  const int KB = K / 64;
+  for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
+       t += (long long)gridDim.x * blockDim.x) {
+    const int s = (int)(t & 1);
+    const int l = (int)((t >> 1) & 31);
+    const int gq = (int)((t >> 6) & 7);
+    const long long chunk = t >> 9;
+    const int kb = (int)(chunk % KB);
+    const int nt = (int)(chunk / KB);
+    uint32_t w = 0;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {  // nibbles p (kept row 0) and p + 4 (kept row 1)
+      const int n = nt * 128 + 16 * gq + (l >> 2) + 8 * (p & 1);
+      const int j = kb * 16 + 8 * s + (l & 3) + 4 * ((p >> 1) & 1);
+      const uint32_t c4 = group_codes(q, N, j, n);
+      bool ok;
+      const uint32_t m = kept_mask(c4, group_zero(zeros, N, group, j, n), &ok);
+      const int i0 = __ffs(m) - 1;
+      const int i1 = __ffs(m & (m - 1u)) - 1;
+      w |= ((c4 >> (4 * i0)) & 0xFu) << (4 * p);
+      w |= ((c4 >> (4 * i1)) & 0xFu) << (4 * (p + 4));
+    }
+    out[t] = w;
+  }
+}
+
+__global__ void sparse_meta_kernel(const uint32_t* __restrict__ q, const uint32_t* __restrict__ zeros,
+                                   int K, int N, int group, uint32_t* __restrict__ out, int* bad,
+                                   long long total) {
+  const int KB = K / 64;
+  for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
+       t += (long long)gridDim.x * blockDim.x) {
+    const int s = (int)(t & 1);
+    const int h = (int)((t >> 1) & 1);
+    const int r = (int)((t >> 2) & 7);
+    const int gq = (int)((t >> 5) & 7);
+    const long long chunk = t >> 8;
+    const int kb = (int)(chunk % KB);
+    const int nt = (int)(chunk / KB);
+    uint32_t w = 0;
+    int nbad = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int n = nt * 128 + 16 * gq + r + 8 * (i >> 2);
+      const int j = kb * 16 + 8 * s + 4 * h + (i & 3);
+      bool ok;
+      const uint32_t m = kept_mask(group_codes(q, N, j, n), group_zero(zeros, N, group, j, n), &ok);
+      nbad += ok ? 0 : 1;
+      const uint32_t i0 = (uint32_t)(__ffs(m) - 1);
+      const uint32_t i1 = (uint32_t)(__ffs(m & (m - 1u)) - 1);
+      w |= (i0 | (i1 << 2)) << (4 * i);
+    }
+    out[t] = w;
+    if (bad && nbad) atomicAdd(bad, nbad);
+  }
+}
+
 int grid_for(long long work, int threads) {
   long long g = (work + threads - 1) / threads;
   if (g > 152 * 16) g = 152 * 16;
@@ -75,6 +179,19 @@ int grid_for(long long work, int threads) {
 cudaError_t launch_repack(const uint32_t* q, uint32_t* out, int K, int N, cudaStream_t stream) {
   const long long total = (long long)K * N / 8;
   repack_codes_kernel<<<grid_for(total, 256), 256, 0, stream>>>(q, out, K, N, total);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sparse_repack(const uint32_t* q, const uint32_t* zeros, int K, int N, int group,
+                                 uint32_t* codes_out, uint32_t* meta_out, int* bad,
+                                 cudaStream_t stream) {
+  const long long chunks = (long long)(N / 128) * (K / 64);
+  sparse_codes_kernel<<<grid_for(chunks * 512, 256), 256, 0, stream>>>(q, zeros, K, N, group, codes_out,
+                                                                     chunks * 512);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  sparse_meta_kernel<<<grid_for(chunks * 256, 256), 256, 0, stream>>>(q, zeros, K, N, group, meta_out,
+                                                                    bad, chunks * 256);
   return cudaGetLastError();
 }
 

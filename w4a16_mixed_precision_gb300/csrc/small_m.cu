@@ -54,10 +54,45 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// One 32-row step of the 2:4-sparse path ("Marlin / GPTQ-Marlin", section
+// "4. Support de la sparsité 2:4 NVIDIA": dequantise, skip the zeros, sparse
+// GEMM).  The lane's code word holds the kept weights of its two columns
+// (r, r + 8) in two groups of four rows (c, c + 4 of the step); dequantised,
+// its four fp16 pairs are the lane's registers of the compressed 16 x 16 A
+// operand.  `e` is the step's index nibbles, supplied by lanes c = 0 (rows
+// 0..15 of the step) and c = 1 (rows 16..31): sparsity selector 0.  One
+// mma.sp per block of 8 tokens; b[nb] holds the lane's eight X values.
+template <int NB>
+__device__ __forceinline__ void dequant_mma_sp(float (&acc)[NB][4], uint32_t w, uint32_t e,
+                                               uint32_t sub_r, uint32_t add_r8, uint32_t s_r,
+                                               uint32_t s_r8, const uint4 (&b)[NB]) {
+  const uint32_t k16 = 0x2C002C00u;  // 1/16 as an fp16 pair
+  uint32_t a0, a1, a2, a3;
+  asm volatile("{\n\t" W4A16_DEQ_PTX("%4", "%5", "%6", "%7", "%8", "%9")
+               "mov.b32 %0, t0;\n\tmov.b32 %1, t1;\n\tmov.b32 %2, t2;\n\tmov.b32 %3, t3;\n\t}"
+               : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+               : "r"(w), "r"(sub_r), "r"(add_r8), "r"(s_r), "r"(s_r8), "r"(k16));
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb)
+    asm volatile(
+        "mma.sp::ordered_metadata.sync.aligned.m16n8k32.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9, %10, %11}, {%0, %1, %2, %3}, %12, 0x0;"
+        : "+f"(acc[nb][0]), "+f"(acc[nb][1]), "+f"(acc[nb][2]), "+f"(acc[nb][3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b[nb].x), "r"(b[nb].y), "r"(b[nb].z),
+          "r"(b[nb].w), "r"(e));
+}
+
 // NB: blocks of 8 tokens (M <= 8*NB).  JPW: 64-row chunks per consumer warp
 // per unit (a unit has 2*JPW chunks; warp half h takes chunks h*JPW .. +JPW-1).
 // ZP: explicit zero points (else the implicit zero 8 is a constant).
-template <int NB, int JPW, bool ZP>
+// SP: 2:4-sparse weights (kept codes + index nibbles, mma.sp).
+template <int NB, int JPW, bool ZP, bool SP>
 __global__ void __launch_bounds__(kSmThreads, 1)
     w4a16_small_m_kernel(const __grid_constant__ CUtensorMap x_map, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -108,11 +143,14 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       const uint8_t* codes = reinterpret_cast<const uint8_t*>(p.codes);
+      const uint8_t* meta = reinterpret_cast<const uint8_t*>(p.meta);
       const int KB = p.K / kChunkK;
-      const uint32_t code_bytes = (uint32_t)(cpu * kChunkCodeBytes);
+      constexpr uint32_t chunk_code = SP ? kSpChunkCodeBytes : kChunkCodeBytes;
+      const uint32_t code_bytes = (uint32_t)cpu * chunk_code;
+      const uint32_t meta_bytes = SP ? (uint32_t)cpu * kSpChunkMetaBytes : 0u;
       const uint32_t scale_bytes = (uint32_t)(p.n_g * kTileN * 2);
       const uint32_t zero_bytes = (uint32_t)(p.n_g * kTileN / 2);
-      const uint32_t tx = code_bytes + scale_bytes + (p.zeros ? zero_bytes : 0u);
+      const uint32_t tx = code_bytes + meta_bytes + scale_bytes + (p.zeros ? zero_bytes : 0u);
       const int upg = p.units_per_group;
       int nt = tile_begin, ku = ku_begin;
       int g = (ku / upg) * p.n_g, ku_in_g = ku - (ku / upg) * upg;
@@ -123,8 +161,9 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
         const uint32_t fb = bar(ctrl->full[s]);
         mbar_arrive_expect_tx(fb, tx);
-        bulk_g2s(st + p.off_codes, codes + ((size_t)nt * KB + (size_t)ku * cpu) * kChunkCodeBytes,
-                 code_bytes, fb, pol);
+        const size_t chunk0 = (size_t)nt * KB + (size_t)ku * cpu;
+        bulk_g2s(st + p.off_codes, codes + chunk0 * chunk_code, code_bytes, fb, pol);
+        if (SP) bulk_g2s(st + p.off_meta, meta + chunk0 * kSpChunkMetaBytes, meta_bytes, fb, pol);
         const size_t grow = (size_t)nt * p.G + g;
         bulk_g2s(st + p.off_scales, p.scales + grow * kTileN, scale_bytes, fb, pol);
         if (p.zeros) bulk_g2s(st + p.off_zeros, p.zeros + grow * (kTileN / 2), zero_bytes, fb, pol);
@@ -173,26 +212,40 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     // xr = sigma(r) = 2(r%4) + r/4 of the block (so the four rows a half-warp
     // reads fall in four different 32-byte bank groups of the 128-byte
     // swizzle), rows k = 16ks + 4c .. +3 = 16-byte unit 2ks + c/2, swizzled by xr.
-    const int xr = ((r & 3) << 1) | (r >> 2);
-    uint32_t xoff[JPW][4];  // stage-relative byte offsets, per chunk and k-step
+    // The sparse path keeps the k order: per 32-row step s, B register j of
+    // lane (r, c) holds rows 32s + 8j + 2c, +1 of token r, i.e. 32-bit word c
+    // of 16-byte unit 4s + j of the token's row (swizzled by r; the eight
+    // tokens of a block then fall in eight different 16-byte columns).
+    const int xr = SP ? r : (((r & 3) << 1) | (r >> 2));
+    constexpr int kXo = SP ? 8 : 4;
+    uint32_t xoff[JPW][kXo];  // stage-relative byte offsets, per chunk and k-step (x unit)
 #pragma unroll
     for (int jj = 0; jj < JPW; ++jj)
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        xoff[jj][ks] = (uint32_t)(h * JPW + jj) * p.x_chunk_bytes + (uint32_t)xr * 128 +
-                       (uint32_t)(c & 1) * 8 + (uint32_t)(((2 * ks + (c >> 1)) ^ xr) << 4);
+      for (int ks = 0; ks < kXo; ++ks) {
+        const uint32_t row0 = (uint32_t)(h * JPW + jj) * p.x_chunk_bytes + (uint32_t)xr * 128;
+        if constexpr (SP)
+          xoff[jj][ks] = row0 + (uint32_t)c * 4 + (uint32_t)((ks ^ xr) << 4);
+        else
+          xoff[jj][ks] = row0 + (uint32_t)(c & 1) * 8 + (uint32_t)(((2 * ks + (c >> 1)) ^ xr) << 4);
+      }
     // stage-relative offsets of this lane's codes, scales and zeros; the
     // warp's chunks lie in one group row: row h of the unit when a unit spans
     // two groups (group 128, 256-row units), else row 0
     const int gsub = (p.n_g > 1) ? h : 0;
-    const uint32_t code_off = p.off_codes + (uint32_t)(h * JPW) * kChunkCodeBytes +
-                              (uint32_t)(g * 32 + lane) * 16;
+    constexpr uint32_t chunk_code = SP ? kSpChunkCodeBytes : kChunkCodeBytes;
+    const uint32_t code_off = p.off_codes + (uint32_t)(h * JPW) * chunk_code +
+                              (uint32_t)(g * 32 + lane) * (SP ? 8 : 16);
+    // sparse: this lane's index words (both 32-row steps of a chunk), the
+    // words of rows 0..15 (c even) or 16..31 (c odd) of each step
+    const uint32_t meta_off = p.off_meta + (uint32_t)(h * JPW) * kSpChunkMetaBytes +
+                              (uint32_t)((g * 8 + r) * 2 + (c & 1)) * 8;
     const uint32_t sc_off = p.off_scales + (uint32_t)(gsub * kTileN + col_r) * 2;
     const uint32_t zr_off = p.off_zeros + (uint32_t)(gsub * (kTileN / 2) + (col_r >> 1));
     const uint32_t z_shift = (uint32_t)(col_r & 1) * 4;
-    // accumulator column 2c + e of a block is token sigma(2c + e)
-    const int tok0 = (((2 * c) & 3) << 1) | ((2 * c) >> 2);
-    const int tok1 = (((2 * c + 1) & 3) << 1) | ((2 * c + 1) >> 2);
+    // accumulator column 2c + e of a block is token sigma(2c + e) (sparse: 2c + e)
+    const int tok0 = SP ? 2 * c : ((((2 * c) & 3) << 1) | ((2 * c) >> 2));
+    const int tok1 = SP ? 2 * c + 1 : ((((2 * c + 1) & 3) << 1) | ((2 * c + 1) >> 2));
     // With two or more token blocks, odd k-steps accumulate into a second set
     // (acc2), so consecutive MMAs of a block do not wait on each other (measured:
     // M = 16 on 16384x19456, 46.1 -> 42.2 us; at NB = 1 it was 2% slower).
@@ -214,8 +267,18 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         if (!wait_warp(bar(ctrl->full[s]), ph, wc)) { ok = false; break; }
         const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
         uint4 wv[JPW];
+        if constexpr (SP) {
+          // x, y: code words of the chunk's two steps; z, w: their index words
 #pragma unroll
-        for (int jj = 0; jj < JPW; ++jj) wv[jj] = lds128(st + code_off + (uint32_t)jj * kChunkCodeBytes);
+          for (int jj = 0; jj < JPW; ++jj) {
+            const uint2 cw = lds64(st + code_off + (uint32_t)jj * kSpChunkCodeBytes);
+            const uint2 mw = lds64(st + meta_off + (uint32_t)jj * kSpChunkMetaBytes);
+            wv[jj] = make_uint4(cw.x, cw.y, mw.x, mw.y);
+          }
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < JPW; ++jj) wv[jj] = lds128(st + code_off + (uint32_t)jj * kChunkCodeBytes);
+        }
         // implicit zero 8: 1024 + 8 and -(64 + 8) as fp16 pairs
         uint32_t sub0 = 0x64086408u, add1 = 0xD480D480u;
         if constexpr (ZP) {
@@ -226,16 +289,35 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         }
         const uint32_t sr = lds_u16(st + sc_off), sr8 = lds_u16(st + sc_off + 16);
         const uint32_t s0 = sr | (sr << 16), s1 = sr8 | (sr8 << 16);
+        if constexpr (SP) {
 #pragma unroll
-        for (int jj = 0; jj < JPW; ++jj) {
-          const uint32_t wk[4] = {wv[jj].x, wv[jj].y, wv[jj].z, wv[jj].w};
+          for (int jj = 0; jj < JPW; ++jj)
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            uint2 b[NB];
+            for (int ks = 0; ks < 2; ++ks) {
+              uint4 b[NB];
 #pragma unroll
-            for (int nb = 0; nb < NB; ++nb) b[nb] = lds64(st + xoff[jj][ks] + (uint32_t)nb * 1024);
-            if (kTwoChains && (ks & 1)) dequant_mma<NB>(acc2, wk[ks], sub0, add1, s0, s1, b);
-            else dequant_mma<NB>(acc, wk[ks], sub0, add1, s0, s1, b);
+              for (int nb = 0; nb < NB; ++nb) {
+                const uint32_t xb = st + (uint32_t)nb * 1024;
+                b[nb] = make_uint4(lds32(xb + xoff[jj][4 * ks]), lds32(xb + xoff[jj][4 * ks + 1]),
+                                   lds32(xb + xoff[jj][4 * ks + 2]), lds32(xb + xoff[jj][4 * ks + 3]));
+              }
+              const uint32_t w = ks ? wv[jj].y : wv[jj].x;
+              const uint32_t e = ks ? wv[jj].w : wv[jj].z;
+              if (kTwoChains && ks) dequant_mma_sp<NB>(acc2, w, e, sub0, add1, s0, s1, b);
+              else dequant_mma_sp<NB>(acc, w, e, sub0, add1, s0, s1, b);
+            }
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < JPW; ++jj) {
+            const uint32_t wk[4] = {wv[jj].x, wv[jj].y, wv[jj].z, wv[jj].w};
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              uint2 b[NB];
+#pragma unroll
+              for (int nb = 0; nb < NB; ++nb) b[nb] = lds64(st + xoff[jj][ks] + (uint32_t)nb * 1024);
+              if (kTwoChains && (ks & 1)) dequant_mma<NB>(acc2, wk[ks], sub0, add1, s0, s1, b);
+              else dequant_mma<NB>(acc, wk[ks], sub0, add1, s0, s1, b);
+            }
           }
         }
         __syncwarp();
@@ -361,17 +443,18 @@ __global__ void __launch_bounds__(kSmThreads, 1)
 
 }  // namespace
 
-#define W4A16_SMALL_M_KERNELS(X)                                                            \
-  X(1, 1, false) X(2, 1, false) X(3, 1, false) X(4, 1, false)                                \
-  X(1, 2, false) X(2, 2, false) X(3, 2, false) X(4, 2, false)                                \
-  X(1, 1, true) X(2, 1, true) X(3, 1, true) X(4, 1, true)                                    \
-  X(1, 2, true) X(2, 2, true) X(3, 2, true) X(4, 2, true)
+#define W4A16_SMALL_M_KERNELS_SP(X, SP)                                                     \
+  X(1, 1, false, SP) X(2, 1, false, SP) X(3, 1, false, SP) X(4, 1, false, SP)                \
+  X(1, 2, false, SP) X(2, 2, false, SP) X(3, 2, false, SP) X(4, 2, false, SP)                \
+  X(1, 1, true, SP) X(2, 1, true, SP) X(3, 1, true, SP) X(4, 1, true, SP)                    \
+  X(1, 2, true, SP) X(2, 2, true, SP) X(3, 2, true, SP) X(4, 2, true, SP)
+#define W4A16_SMALL_M_KERNELS(X) W4A16_SMALL_M_KERNELS_SP(X, false) W4A16_SMALL_M_KERNELS_SP(X, true)
 
 cudaError_t small_m_set_smem_limit(int bytes) {
   cudaError_t e = cudaSuccess;
-#define W4A16_SET(NB, JPW, ZP)                                                               \
+#define W4A16_SET(NB, JPW, ZP, SP)                                                           \
   if (e == cudaSuccess)                                                                      \
-    e = cudaFuncSetAttribute(w4a16_small_m_kernel<NB, JPW, ZP>,                              \
+    e = cudaFuncSetAttribute(w4a16_small_m_kernel<NB, JPW, ZP, SP>,                          \
                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   W4A16_SMALL_M_KERNELS(W4A16_SET)
 #undef W4A16_SET
@@ -379,7 +462,7 @@ cudaError_t small_m_set_smem_limit(int bytes) {
 }
 
 cudaError_t launch_small_m(const CUtensorMap& x_map, const GemmParams& p, int grid,
-                           uint32_t smem_bytes, cudaStream_t stream) {
+                           uint32_t smem_bytes, bool sparse, cudaStream_t stream) {
   const int nb = p.bn / 8, jpw = p.cpu / 2;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -392,9 +475,9 @@ cudaError_t launch_small_m(const CUtensorMap& x_map, const GemmParams& p, int gr
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const bool zp = p.zeros != nullptr;
-#define W4A16_LAUNCH(NB, JPW, ZP)                                                          \
-  if (nb == NB && jpw == JPW && zp == ZP)                                                  \
-    return cudaLaunchKernelEx(&cfg, w4a16_small_m_kernel<NB, JPW, ZP>, x_map, p);
+#define W4A16_LAUNCH(NB, JPW, ZP, SP)                                                      \
+  if (nb == NB && jpw == JPW && zp == ZP && sparse == SP)                                  \
+    return cudaLaunchKernelEx(&cfg, w4a16_small_m_kernel<NB, JPW, ZP, SP>, x_map, p);
   W4A16_SMALL_M_KERNELS(W4A16_LAUNCH)
 #undef W4A16_LAUNCH
   return cudaErrorInvalidValue;

@@ -34,6 +34,7 @@ class Problem:
     N: int
     group: int          # 128, or K for one scale per column
     asym: bool          # explicit 4-bit zeros (True) or implicit zero 8 (False)
+    sparse: bool = False  # 2:4-sparse weights, multiplied on the sparse path
 
     @property
     def G(self) -> int:
@@ -44,8 +45,10 @@ class Problem:
         return f"{self.cfg}:{self.M}:{self.K}:{self.N}:{self.group}:{int(self.asym)}"
 
     def algorithmic_bytes(self) -> int:
-        """Bytes the method must move: codes + scales (+ zeros) + X + Y."""
-        b = self.K * self.N // 2 + self.G * self.N * 2 + 2 * self.M * self.K + 2 * self.M * self.N
+        """Bytes the method must move: codes + scales (+ zeros) + X + Y.  2:4
+        weights: the kept half of the codes plus a 4-bit index pair per four."""
+        codes = self.K * self.N // 4 + self.K * self.N // 8 if self.sparse else self.K * self.N // 2
+        b = codes + self.G * self.N * 2 + 2 * self.M * self.K + 2 * self.M * self.N
         if self.asym:
             b += self.G * self.N // 2
         return b
@@ -69,6 +72,9 @@ class Inputs:
 def make_inputs(p: Problem, seed: int | None = None) -> Inputs:
     rng = np.random.default_rng(seed_for(p.key) if seed is None else seed)
     X = rng.standard_normal((p.M, p.K), dtype=np.float32).astype(np.float16)
+    if p.sparse:
+        Qp, S, Zp = make_sparse_weights(p.K, p.N, p.group, p.asym, seed=int(rng.integers(2**32)))
+        return Inputs(X, Qp, S, Zp)
     Qp = rng.integers(0, 2**32, size=(p.K // 8, p.N), dtype=np.uint64).astype(np.uint32).view(np.int32)
     S = (0.02 * rng.uniform(0.5, 1.5, size=(p.G, p.N))).astype(np.float16)
     Zp = None
@@ -169,6 +175,11 @@ ODD_SHAPES = [(2048, 2048), (2048, 5632), (5120, 15360), (13824, 5120)]
 ODD_M = [1, 16, 48]
 ASYM_ODD = [Problem("asym-odd", M, K, N, g, True)
             for (K, N) in ODD_SHAPES for M in ODD_M for g in (128, K)]
+
+# the 7B decode linears with 2:4-sparse weights (the sparse path serves M <= 32)
+SPARSE_7B_DECODE = [Problem("sparse-7b-decode", M, K, N, 128, False, True)
+                    for (K, N) in LLAMA7B_DECODE_SHAPES for M in LLAMA7B_DECODE_M]
+SPARSE_CONFIGS = {"sparse-7b-decode": SPARSE_7B_DECODE}
 
 ALL_CONFIGS = {
     "single": SMALL,
