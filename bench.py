@@ -348,7 +348,7 @@ def run_gpu(args, problems, rank, world, local):
         tq, ts = torch.from_numpy(Qp).to(dev), torch.from_numpy(S).to(dev)
         tz = torch.from_numpy(Zp).to(dev) if a else None
         pw = w4.sparse_repack(tq, ts, tz, g) if sparse else w4.repack(tq, ts, tz, g)
-        if sparse:
+        if sparse and not args.no_table:
             # the same weights in the dense layout, for the per-run comparison
             dense_pw[(K, N, g, a)] = w4.repack(tq, ts, tz, g)
         copies = [pw]
@@ -358,7 +358,7 @@ def run_gpu(args, problems, rank, world, local):
         for _ in range(n_copies - 1):
             copies.append(dataclasses.replace(pw, buf=pw.buf.clone()))
         packed[(K, N, g, a)] = copies
-        if sparse:
+        if sparse and not args.no_table:
             dense_pw[(K, N, g, a)] = [dense_pw[(K, N, g, a)]] + [
                 dataclasses.replace(dense_pw[(K, N, g, a)], buf=dense_pw[(K, N, g, a)].buf.clone())
                 for _ in range(max(1, -(-2 * L2_BYTES // (K * N // 2))) )]
@@ -607,8 +607,8 @@ def end_to_end(problems, packed, ws, plans, dev, args, step_bytes, call):
     dt = (time.perf_counter() - t0) / steps
     return {"value": step_bytes / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": xt * 2,
             "d2h_bytes_per_step": yt * 2, "ms_per_step": dt * 1e3, "steps": steps,
-            "path": "per step: one H2D copy of all activations from pinned host memory, the 24 "
-                    "marlin_gemm calls through the Python binding, one D2H copy of all outputs; "
+            "path": f"per step: one H2D copy of all activations from pinned host memory, the {len(problems)} "
+                    f"library calls ({call.__name__}) through the Python binding, one D2H copy of all outputs; "
                     "host wall clock around the whole step, synchronised"}
 
 
