@@ -632,8 +632,10 @@ def main():
     if args.shape:
         v = [int(t) for t in args.shape.split(",")]
         M, K, N = v[0], v[1], v[2]
-        problems = [Problem("shape", M, K, N, v[3] if len(v) > 3 else 128, bool(v[4]) if len(v) > 4 else False)]
-        args.workload = f"shape {M}x{K}x{N}"
+        sparse = args.workload in SPARSE_CONFIGS
+        problems = [Problem("shape", M, K, N, v[3] if len(v) > 3 else 128, bool(v[4]) if len(v) > 4 else False,
+                            sparse)]
+        args.workload = f"shape {M}x{K}x{N}" + (" 2:4-sparse" if sparse else "")
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
         run_reference(args, problems, rank, int(os.environ.get("WORLD_SIZE", "1")))

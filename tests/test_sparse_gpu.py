@@ -209,3 +209,30 @@ def test_sparse_full_size_sampled(p):
     y_ref = oracle.w4a16_sparse(X, kc, ki, S, Zp, p.group, p.N, idx=idx)
     ok, err, ratio = oracle.within_tolerance(y.ravel()[idx], y_ref)
     assert ok, f"{p.key}: max abs err {err}, worst ratio {ratio}"
+
+
+def test_sparse_linear_layer():
+    """The layer with sparse=True: M <= 32 on the 2:4 path, larger M on the dense
+    kernel; both within tolerance of the oracle, and equal to the dense layer's
+    output where both use the same kernel."""
+    from w4a16_mixed_precision_gb300.layer import W4A16Linear
+    K, N, g = 1024, 640, 128
+    Qp, S, Zp = make_sparse_weights(K, N, g, True, seed=51)
+    lay_sp = W4A16Linear(torch.from_numpy(Qp), torch.from_numpy(S), torch.from_numpy(Zp), g, sparse=True)
+    lay_de = W4A16Linear(torch.from_numpy(Qp), torch.from_numpy(S), torch.from_numpy(Zp), g)
+    for M in (4, 32, 40):
+        X = make_activations(M, K, seed=M)
+        x = _dev(X)
+        y_sp = lay_sp(x.reshape(1, M, K)).reshape(M, N).cpu().numpy()
+        y_de = lay_de(x).cpu().numpy()
+        y_ref = oracle.w4a16(X, Qp, S, Zp, g, N)
+        for y in (y_sp, y_de):
+            ok, err, ratio = oracle.within_tolerance(y, y_ref)
+            assert ok, f"M={M}: max abs err {err}, worst ratio {ratio}"
+        if M > 32:
+            assert np.array_equal(y_sp.view(np.uint16), y_de.view(np.uint16))
+    Qd, Sd, _ = make_sparse_weights(K, N, g, False, seed=52)
+    Qd = Qd.copy()
+    Qd[0, :] = 0x12345678                     # rows 0..7: more than two non-zero codes per group
+    with pytest.raises(ValueError):
+        W4A16Linear(torch.from_numpy(Qd), torch.from_numpy(Sd), None, g, sparse=True)

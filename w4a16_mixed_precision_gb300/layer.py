@@ -7,24 +7,32 @@ suitably prepared weights and scales may also call the kernel directly) and repa
 GPTQ-Marlin", section "Tiled layout et repacking").  Here construction repacks
 once on the GPU and every forward call is one marlin_gemm launch; there is no
 bias and no other arithmetic outside the kernel.
+
+With sparse=True the weights must be 2:4 ("Marlin", section "支持 2:4 稀疏加速":
+two of every four weights zero at fixed positions): the layer also holds the
+2:4 form and serves batches of up to 32 rows with marlin_sparse_gemm, larger
+ones with the dense kernel.
 """
 from __future__ import annotations
 
 import numpy as np
 import torch
 
-from . import Workspace, gemm_into, repack
+from . import Workspace, gemm_into, repack, sparse_gemm_into, sparse_repack
 from .formats import awq_to_gptq
 
 
 class W4A16Linear(torch.nn.Module):
     """y[..., N] = x[..., K] . dequant(W)[K, N], fp16 in and out, fp32 accumulation."""
 
+    SPARSE_MAX_M = 32  # largest batch of the 2:4 path (the warp-level kernel's range)
+
     def __init__(self, qweight: torch.Tensor, scales: torch.Tensor, qzeros: torch.Tensor | None = None,
-                 group: int = 128, device=None):
+                 group: int = 128, device=None, sparse: bool = False):
         """qweight: GPTQ-order int32 [K/8, N]; scales fp16 [K/group, N]; qzeros
         int32 [K/group, N/8] or None (z = 8); group 128, a multiple of 128
-        dividing K, or -1/K for one scale per column."""
+        dividing K, or -1/K for one scale per column.  sparse: the weights are
+        2:4 (raises otherwise); batches of M <= 32 use the sparse path."""
         super().__init__()
         dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
         q = qweight.to(dev, torch.int32).contiguous()
@@ -33,6 +41,7 @@ class W4A16Linear(torch.nn.Module):
         self.K, self.N = q.shape[0] * 8, q.shape[1]
         self.group = self.K if group == -1 else group
         self.packed = repack(q, s, z, self.group)
+        self.sparse_packed = sparse_repack(q, s, z, self.group) if sparse else None
         self._ws = None
         self._ws_m = 0
 
@@ -56,6 +65,9 @@ class W4A16Linear(torch.nn.Module):
         lead = x.shape[:-1]
         x2 = x.reshape(-1, self.K).contiguous()
         y = torch.empty((x2.shape[0], self.N), dtype=torch.float16, device=x2.device)
-        if x2.shape[0] > 0:
-            gemm_into(x2, self.packed, self._workspace(x2.shape[0]), y)
+        M = x2.shape[0]
+        if M > 0 and self.sparse_packed is not None and M <= self.SPARSE_MAX_M:
+            sparse_gemm_into(x2, self.sparse_packed, self._workspace(M), y)
+        elif M > 0:
+            gemm_into(x2, self.packed, self._workspace(M), y)
         return y.reshape(*lead, self.N)
