@@ -51,3 +51,29 @@ def test_expired_wait_is_reported_and_context_survives(M):
     assert w4.device_status(ws) == 0
     ok, err, ratio = oracle.within_tolerance(y.cpu().numpy(), oracle.w4a16(inp.X, inp.Qp, inp.S, None, 128, p.N))
     assert ok, f"max abs err {err}"
+
+
+def test_expired_wait_on_the_sparse_path():
+    """The same on the 2:4-sparse path (the sparse instantiation of the
+    warp-level kernel shares its bounded waits)."""
+    import w4a16_mixed_precision_gb300 as w4
+    from w4a16_mixed_precision_gb300 import _binding as b
+    from workloads import make_activations, make_sparse_weights
+    M, K, N, g = 4, 4096, 1024, 128
+    Qp, S, _ = make_sparse_weights(K, N, g, False, seed=77)
+    X = make_activations(M, K, seed=78)
+    dev = torch.device("cuda", 0)
+    pw = w4.sparse_repack(torch.from_numpy(Qp).to(dev), torch.from_numpy(S).to(dev), None, g)
+    x = torch.from_numpy(X).to(dev)
+    ws = w4.Workspace(M, K, N, g)
+    ws.buf[256:256 + 4 * (N // 128)].view(torch.int32).fill_(-1000000)
+    w4.sparse_gemm(x, pw, ws)
+    torch.cuda.synchronize()
+    rc = b.last_device_status(ws.ptr, torch.cuda.current_stream().cuda_stream)
+    assert rc == b.ERR_TIMEOUT, b.status_string(rc)
+    ws.buf.zero_()
+    y = w4.sparse_gemm(x, pw, ws)
+    torch.cuda.synchronize()
+    assert w4.device_status(ws) == 0
+    ok, err, ratio = oracle.within_tolerance(y.cpu().numpy(), oracle.w4a16(X, Qp, S, None, g, N))
+    assert ok, f"max abs err {err}"

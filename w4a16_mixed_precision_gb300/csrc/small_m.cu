@@ -29,6 +29,11 @@
 //     block.
 //   * Every wait is bounded; on expiry the kernel records a timeout in the
 //     status word and returns.
+//   * The SP instantiation multiplies 2:4-sparse weights ("Marlin", section
+//     "支持 2:4 稀疏加速"): a stage carries the kept half of the codes plus a
+//     4-bit index pair per group of four rows, each consumer step covers 32
+//     rows with one dequantised code word and one mma.sp per token block, and
+//     X keeps its k order (no token permutation).
 #include "common.cuh"
 
 namespace w4a16 {
