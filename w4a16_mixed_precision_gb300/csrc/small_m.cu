@@ -33,7 +33,8 @@
 //     "支持 2:4 稀疏加速"): a stage carries the kept half of the codes plus a
 //     4-bit index pair per group of four rows, each consumer step covers 32
 //     rows with one dequantised code word and one mma.sp per token block, and
-//     X keeps its k order (no token permutation).
+//     X keeps its k order (no token permutation; one ldmatrix.x4 per token
+//     block and step).
 #include "common.cuh"
 
 namespace w4a16 {
@@ -59,9 +60,14 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   return v;
 }
 
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+// Four 8x8 b16 matrices; lanes 8i..8i+7 give the row addresses of matrix i
+// (16 bytes each), and lane l receives row l/4, elements 2(l%4), +1 of each.
+__device__ __forceinline__ uint4 ldmatrix_x4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
   return v;
 }
 
@@ -218,19 +224,20 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     // reads fall in four different 32-byte bank groups of the 128-byte
     // swizzle), rows k = 16ks + 4c .. +3 = 16-byte unit 2ks + c/2, swizzled by xr.
     // The sparse path keeps the k order: per 32-row step s, B register j of
-    // lane (r, c) holds rows 32s + 8j + 2c, +1 of token r, i.e. 32-bit word c
-    // of 16-byte unit 4s + j of the token's row (swizzled by r; the eight
-    // tokens of a block then fall in eight different 16-byte columns).
-    const int xr = SP ? r : (((r & 3) << 1) | (r >> 2));
-    constexpr int kXo = SP ? 8 : 4;
-    uint32_t xoff[JPW][kXo];  // stage-relative byte offsets, per chunk and k-step (x unit)
+    // lane (r, c) holds rows 32s + 8j + 2c, +1 of token r, which is what
+    // ldmatrix.x4 delivers when lane l points at 16-byte unit 4s + l/8 of token
+    // l%8's row (swizzled by the token; the eight rows of each matrix then fall
+    // in eight different 16-byte columns).
+    const int xr = SP ? (lane & 7) : (((r & 3) << 1) | (r >> 2));
+    constexpr int kXo = SP ? 2 : 4;
+    uint32_t xoff[JPW][kXo];  // stage-relative byte offsets, per chunk and k-step
 #pragma unroll
     for (int jj = 0; jj < JPW; ++jj)
 #pragma unroll
       for (int ks = 0; ks < kXo; ++ks) {
         const uint32_t row0 = (uint32_t)(h * JPW + jj) * p.x_chunk_bytes + (uint32_t)xr * 128;
         if constexpr (SP)
-          xoff[jj][ks] = row0 + (uint32_t)c * 4 + (uint32_t)((ks ^ xr) << 4);
+          xoff[jj][ks] = row0 + (uint32_t)(((4 * ks + (lane >> 3)) ^ xr) << 4);
         else
           xoff[jj][ks] = row0 + (uint32_t)(c & 1) * 8 + (uint32_t)(((2 * ks + (c >> 1)) ^ xr) << 4);
       }
@@ -301,11 +308,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
             for (int ks = 0; ks < 2; ++ks) {
               uint4 b[NB];
 #pragma unroll
-              for (int nb = 0; nb < NB; ++nb) {
-                const uint32_t xb = st + (uint32_t)nb * 1024;
-                b[nb] = make_uint4(lds32(xb + xoff[jj][4 * ks]), lds32(xb + xoff[jj][4 * ks + 1]),
-                                   lds32(xb + xoff[jj][4 * ks + 2]), lds32(xb + xoff[jj][4 * ks + 3]));
-              }
+              for (int nb = 0; nb < NB; ++nb) b[nb] = ldmatrix_x4(st + xoff[jj][ks] + (uint32_t)nb * 1024);
               const uint32_t w = ks ? wv[jj].y : wv[jj].x;
               const uint32_t e = ks ? wv[jj].w : wv[jj].z;
               if (kTwoChains && ks) dequant_mma_sp<NB>(acc2, w, e, sub0, add1, s0, s1, b);
