@@ -48,7 +48,7 @@ typedef struct CUstream_st* marlin_stream_t; /* same type as cudaStream_t */
 typedef enum {
   MARLIN_OK = 0,
   MARLIN_ERR_INVALID_ARG = 1,          /* bad shape, group, NULL pointer          */
-  MARLIN_ERR_UNSUPPORTED = 2,          /* valid request this build cannot serve   */
+  MARLIN_ERR_UNSUPPORTED = 2,          /* valid request this library cannot serve */
   MARLIN_ERR_MISALIGNED = 3,           /* a pointer is not 16-byte aligned        */
   MARLIN_ERR_WORKSPACE_TOO_SMALL = 4,  /* workspace smaller than required        */
   MARLIN_ERR_CUDA = 5,                 /* a CUDA runtime call or launch failed    */
@@ -136,7 +136,7 @@ marlin_status_t marlin_gemm(const uint16_t* X, const void* packed, const uint16_
 
 /*
  * Which fused kernel marlin_gemm_ex launches.  The pages' kernel is one
- * design; this build has two for the same operation: a warp-level one
+ * design; this library has two for the same operation: a warp-level one
  * (mma.sync fed from registers, M <= 32) and a tcgen05 one (operand in tensor
  * memory, any M).  MARLIN_KERNEL_AUTO picks by M (the warp-level kernel for
  * M <= 24, or the bound set by the environment variable W4A16_SMALL_M_MAX,
