@@ -285,7 +285,9 @@ marlin_status_t marlin_sparse_repack(const int32_t* q, const uint16_t* scales, c
  * workspace sized by marlin_workspace_bytes(M, K, N, group, ...) serves this
  * call too.  M > 32 -> MARLIN_ERR_UNSUPPORTED.  Results agree with
  * marlin_gemm's on the expanded weights within the parity tolerance (the
- * fp32 summation orders differ).
+ * fp32 summation orders differ).  Only the kept terms enter the sum, so for
+ * an inf or NaN in X at a dropped row the result is not specified here (the
+ * dense product gives NaN there; a sum over the kept terms stays finite).
  */
 marlin_status_t marlin_sparse_gemm(const uint16_t* X, const void* packed, const void* meta,
                                    const uint16_t* scales, const int32_t* zeros, uint16_t* Y, int M,

@@ -134,3 +134,23 @@ def test_tile_layout_round_trip(oracle_lib):
     Pc1, _ = oracle_lib.sparse_repack(one, np.zeros_like(ki), K, N)
     nz = np.flatnonzero(Pc1)
     assert nz.size == 1 and bin(int(Pc1[nz[0]]) & 0xFFFFFFFF).count("1") == 2
+
+
+def test_non_finite_x_at_a_dropped_row(oracle_lib):
+    """The 2:4 product skips the dropped terms: a NaN or inf in X at a dropped
+    row does not reach Y (the dense sum would give inf * 0 = NaN there); at a
+    kept row it propagates as in the dense product."""
+    K, N, M, g = 128, 8, 2, 128
+    q = np.full((K, N), 8, np.uint8)
+    q[1, :] = 9                               # every column keeps rows 0 and 1 of group 0
+    S = np.ones((1, N), np.float16)
+    Qp = wl.pack_codes(q)
+    kc, ki, bad = oracle_lib.sparse_compress(Qp, None, K, N, g)
+    assert bad == 0 and np.all(ki[0] == (0 | 1 << 2))
+    X = np.ones((M, K), np.float16)
+    X[0, 2] = np.inf                          # row 2: dropped
+    X[1, 1] = np.nan                          # row 1: kept
+    y_sp = oracle_lib.w4a16_sparse(X, kc, ki, S, None, g, N)
+    y_de = oracle_lib.w4a16(X, Qp, S, None, g, N)
+    assert np.all(y_sp[0] == 1.0) and np.all(np.isnan(y_de[0]))
+    assert np.all(np.isnan(y_sp[1])) and np.all(np.isnan(y_de[1]))
