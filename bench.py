@@ -208,6 +208,16 @@ def dist_barrier(world: int):
 
 # ---- CPU oracle baseline ------------------------------------------------------------
 
+def host_cores() -> int:
+    """Cores this process may run on (its affinity mask, which a cgroup or
+    taskset narrows), used both as the oracle's thread count and as the
+    reported core count."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
 class OracleSampler:
     """Times the CPU oracle (as it stands) on column samples of the workload.
 
@@ -280,7 +290,7 @@ def oracle_baseline(problems, budget_s: float, threads: int):
 def run_reference(args, problems, rank, world):
     if rank != 0:
         return
-    threads = os.cpu_count() or 1
+    threads = host_cores()
     smp = OracleSampler(threads)
     steps = args.steps + args.warmup
     budget = max(0.02, min(10.0, 90.0 / max(steps, 1)))
@@ -482,7 +492,7 @@ def run_gpu(args, problems, rank, world, local):
                                            f"{tf / peaks['bf16_tflops']:.3f}",
                             "kernel": kernel_names(problems)}
     if rank == 0 and not args.no_cpu_baseline:
-        threads = os.cpu_count() or 1
+        threads = host_cores()
         v, s, desc = oracle_baseline(problems, args.cpu_budget, threads)
         line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
                                 "sample": desc, "seconds": s}

@@ -30,7 +30,10 @@
  *   zeros   int32 [K/group][N/8]; bits 4j..4j+3 of word [g][c] hold z[g][8c+j]
  *           (stored literally, no offset).  NULL means z = 8 everywhere.
  *   group   128, any multiple of 128 that divides K, or K (or -1 meaning K)
- *           for one scale per column.
+ *           for one scale per column.  A group that divides K but is not a
+ *           multiple of 128 (32, 64) -> MARLIN_ERR_UNSUPPORTED ("Marlin",
+ *           section "Group size 为什么是 128": 64 and 256 run slower and 32
+ *           may not run); any other group -> MARLIN_ERR_INVALID_ARG.
  *   Shapes  K % 128 == 0, N % 128 == 0, M >= 0 (M == 0 is a no-op).
  */
 #ifndef W4A16_GB300_MARLIN_H
@@ -48,19 +51,24 @@ typedef struct CUstream_st* marlin_stream_t; /* same type as cudaStream_t */
 typedef enum {
   MARLIN_OK = 0,
   MARLIN_ERR_INVALID_ARG = 1,          /* bad shape, group, NULL pointer          */
-  MARLIN_ERR_UNSUPPORTED = 2,          /* valid request this library cannot serve */
+  MARLIN_ERR_UNSUPPORTED = 2,          /* valid request this library cannot serve
+                                          (group 32/64, M > 32 on the warp path)   */
   MARLIN_ERR_MISALIGNED = 3,           /* a pointer is not 16-byte aligned        */
   MARLIN_ERR_WORKSPACE_TOO_SMALL = 4,  /* workspace smaller than required        */
   MARLIN_ERR_CUDA = 5,                 /* a CUDA runtime call or launch failed    */
   MARLIN_ERR_TIMEOUT = 6               /* a bounded wait inside a kernel gave up  */
 } marlin_status_t;
 
-/* Human-readable name of a status code (static string, never NULL). */
+/* Human-readable name of a status code (static string, never NULL).  No page
+ * passage: housekeeping of this library, not the method's arithmetic. */
 const char* marlin_status_string(marlin_status_t status);
 
 /*
  * Size and offsets of the single repacked weight buffer, laid out as
- * [codes | scales | zeros]:
+ * [codes | scales | zeros].  The pages fix no format for the repacked weights
+ * ("Marlin / GPTQ-Marlin", section "Tiled layout et repacking", says only that
+ * they are rewritten into a tiled layout); this is the size query for this
+ * library's own layout:
  *   codes  K*N/2 bytes in this library's tile layout (see marlin_repack);
  *   scales fp16, K*N/group values, at *off_scales (tile-major, see marlin_repack);
  *   zeros  K*N/(2*group) bytes at *off_zeros (only if has_zeros; *off_zeros =
@@ -98,12 +106,14 @@ marlin_status_t marlin_repack(const int32_t* q, const uint16_t* scales, const in
 
 /*
  * Bytes of device workspace marlin_gemm needs for this problem on `device`
- * (its SM count sets the partition).  The workspace holds the fp32 partial
- * tiles of the striped partition's global reduction, one arrival counter per
- * output tile and a status word.  A buffer sized for M also serves every
- * smaller M with the same K, N, group, with either kernel (marlin_gemm_ex).
- * Host-only; queries the device
- * attributes once.  bytes: host pointer, written.
+ * (its SM count sets the partition).  "Marlin Project Overview", section
+ * "Key Techniques", item "Striped Partitioning", names the global reduction
+ * this scratch serves; the size query itself has no page passage.
+ * The workspace holds one fp32 partial tile per CTA for the striped
+ * partition's global reduction, one arrival counter per output tile and a
+ * status word.  A buffer sized for M also serves every smaller M with the
+ * same K, N, group, with either kernel (marlin_gemm_ex).  Host-only; queries
+ * the device attributes once.  bytes: host pointer, written.
  */
 marlin_status_t marlin_workspace_bytes(int M, int K, int N, int group, int device, size_t* bytes);
 
@@ -126,6 +136,14 @@ marlin_status_t marlin_workspace_bytes(int M, int K, int N, int group, int devic
  *            Calls that share a workspace must be ordered (same stream, or
  *            events): concurrent calls on one workspace race.
  * Result is deterministic: the same inputs give bit-identical Y on every run.
+ * Weights (packed, scales, zeros) are treated as constant: the kernel may
+ * start streaming them before the previous kernel on `stream` has finished
+ * (programmatic dependent launch); X, Y and workspace are touched only after
+ * it has.  So the weight buffers must not be written by a kernel that is
+ * still running when this call is enqueued.  Writes by marlin_repack /
+ * marlin_sparse_repack, by copies, or by any kernel that does not trigger
+ * its dependents early are complete in time.  The environment variable
+ * W4A16_EARLY_WEIGHTS=0 makes the kernels wait before reading anything.
  * Errors: INVALID_ARG, MISALIGNED, WORKSPACE_TOO_SMALL (host checks, nothing
  * launched); CUDA (launch failure).  A bounded wait that expires inside the
  * kernel is reported later by marlin_last_device_status.
@@ -176,9 +194,9 @@ marlin_status_t marlin_gemm_ex(const uint16_t* X, const void* packed, const uint
  *
  * Arguments as for marlin_gemm, without workspace.  Results are identical to
  * marlin_gemm's for the same inputs.
- * Limit: problems whose marlin_workspace_bytes exceeds 8 MiB (on a 152-SM
- * GB300, M > 48) return MARLIN_ERR_WORKSPACE_TOO_SMALL before anything is
- * launched; other argument errors as for marlin_gemm.
+ * Limit: problems whose scratch exceeds 8 MiB (on a 152-SM GB300, M > 96)
+ * return MARLIN_ERR_WORKSPACE_TOO_SMALL before anything is launched; other
+ * argument errors as for marlin_gemm.
  * Set-up: the first call on a device looks up the array's device address
  * (once per device, with that device current); make that first call before
  * any stream capture.  Each call clears the part of the array it uses (status
@@ -295,6 +313,7 @@ marlin_status_t marlin_sparse_gemm(const uint16_t* X, const void* packed, const 
                                    marlin_stream_t stream);
 
 /*
+ * No page passage: failure reporting of this library's bounded waits.
  * Synchronises `stream`, reads and clears the device status word that
  * marlin_gemm keeps in `workspace`, and returns MARLIN_OK or
  * MARLIN_ERR_TIMEOUT (a bounded wait in a kernel expired; that call's Y is

@@ -52,10 +52,17 @@ def test_packed_layout(lib):
     assert s % 256 == 0 and z % 256 == 0
     b1, _, _ = _binding.packed_layout(2048, 5632, -1, True)
     assert b1 == b
-    for bad in [(100, 128, 128), (128, 100, 128), (256, 128, 64), (384, 128, 256), (0, 128, 128)]:
+    for bad in [(100, 128, 128), (128, 100, 128), (384, 128, 256), (0, 128, 128), (256, 128, 0),
+                (256, 128, 96)]:
         with pytest.raises(_binding.MarlinError) as e:
             _binding.packed_layout(*bad, False)
         assert e.value.status == _binding.ERR_INVALID_ARG
+    # groups of 32 or 64 divide K but are not served ("Marlin", section
+    # "Group size 为什么是 128": 64 runs slower, 32 may not run)
+    for small in [(256, 128, 64), (256, 128, 32)]:
+        with pytest.raises(_binding.MarlinError) as e:
+            _binding.packed_layout(*small, False)
+        assert e.value.status == _binding.ERR_UNSUPPORTED
 
 
 def test_gemm_host_checks(lib):
@@ -67,7 +74,8 @@ def test_gemm_host_checks(lib):
     assert b.gemm_raw(good, good, good, None, good, -1, 256, 256, 128, good, 1 << 20, 0) == b.ERR_INVALID_ARG
     assert b.gemm_raw(good, good, good, None, good, 4, 200, 256, 128, good, 1 << 20, 0) == b.ERR_INVALID_ARG
     assert b.gemm_raw(good, good, good, None, good, 4, 256, 200, 128, good, 1 << 20, 0) == b.ERR_INVALID_ARG
-    assert b.gemm_raw(good, good, good, None, good, 4, 256, 256, 64, good, 1 << 20, 0) == b.ERR_INVALID_ARG
+    assert b.gemm_raw(good, good, good, None, good, 4, 256, 256, 64, good, 1 << 20, 0) == b.ERR_UNSUPPORTED
+    assert b.gemm_raw(good, good, good, None, good, 4, 256, 256, 0, good, 1 << 20, 0) == b.ERR_INVALID_ARG
     assert b.gemm_raw(0, good, good, None, good, 4, 256, 256, 128, good, 1 << 20, 0) == b.ERR_INVALID_ARG
     assert b.gemm_raw(good, good, good, None, good, 4, 256, 256, 128, 0, 1 << 20, 0) == b.ERR_INVALID_ARG
     assert b.gemm_raw(good + 8, good, good, None, good, 4, 256, 256, 128, good, 1 << 20, 0) == b.ERR_MISALIGNED
@@ -107,10 +115,13 @@ def test_sparse_packed_layout(lib):
     assert m % 256 == 0 and s % 256 == 0 and z % 256 == 0
     assert m >= 2048 * 5632 // 4 and s >= m + 2048 * 5632 // 8
     assert z == s + 5632 * 2 and b == z + 5632 // 2
-    for bad in [(100, 128, 128), (256, 128, 64), (0, 128, 128)]:
+    for bad in [(100, 128, 128), (0, 128, 128)]:
         with pytest.raises(_binding.MarlinError) as e:
             _binding.sparse_packed_layout(*bad, False)
         assert e.value.status == _binding.ERR_INVALID_ARG
+    with pytest.raises(_binding.MarlinError) as e:
+        _binding.sparse_packed_layout(256, 128, 64, False)
+    assert e.value.status == _binding.ERR_UNSUPPORTED
 
 
 def test_sparse_host_checks(lib):

@@ -3,13 +3,14 @@
 marlin_gemm_no_alloc keeps its scratch in a static array of the library instead
 of a caller-provided workspace, for operators whose host framework owns all
 device memory or whose path cannot afford cudaMalloc's synchronisation.  Its
-results must match marlin_gemm's (called through the C ABI with a workspace)
-within the parity tolerance, on consecutive calls that reuse the shared array.
+results must be bit-identical to marlin_gemm's (called through the C ABI with a
+workspace: same kernel, same fixed reduction order), on consecutive calls that
+reuse the shared array, and both must match the CPU oracle within the parity
+tolerance.
 
 This file is collected last so that a run stopping at the first failure has
 already run every other test; it also passes alone in a fresh process.
 """
-import numpy as np
 import pytest
 
 import oracle
@@ -57,20 +58,26 @@ def _with_workspace(pw, x, p):
 
 
 def test_no_alloc_matches_workspace_entry_point_on_consecutive_calls():
-    # split column tiles (counters and partials in the shared array), then a
-    # different shape with explicit zeros, then the first one again
+    # split column tiles (counters and partials in the shared array) on the
+    # warp-level kernel, a different shape with explicit zeros, a batch of 80
+    # tokens on the tcgen05 kernel (near the array's limit), then the first
+    # problem again
     problems = [Problem("noalloc", 16, 4096, 4096, 128, False),
                 Problem("noalloc", 5, 2048, 1024, 128, True),
+                Problem("noalloc", 80, 4096, 4096, 128, False),
                 Problem("noalloc", 16, 4096, 4096, 128, False)]
     for p in problems:
         pw, x = _prepared(p)
-        y_ref = _with_workspace(pw, x, p).cpu().numpy().astype(np.float64)
+        y_ws = _with_workspace(pw, x, p).cpu()
         y_a = _no_alloc(pw, x, p)
         y_b = _no_alloc(pw, x, p)       # two calls in a row on the same scratch
         torch.cuda.synchronize()
         for y in (y_a, y_b):
-            ok, err, ratio = oracle.within_tolerance(y.cpu().numpy(), y_ref)
-            assert ok, f"{p.key}: max abs err {err}, worst ratio {ratio}"
+            assert torch.equal(y.cpu(), y_ws), f"{p.key}: differs from marlin_gemm"
+        inp = make_inputs(p)
+        y_ref = oracle.w4a16(inp.X, inp.Qp, inp.S, inp.Zp, p.group, p.N)
+        ok, err, ratio = oracle.within_tolerance(y_ws.numpy(), y_ref)
+        assert ok, f"{p.key}: max abs err {err}, worst ratio {ratio}"
 
 
 def test_no_alloc_rejects_problems_beyond_its_scratch():

@@ -29,6 +29,16 @@ def _stream() -> int:
     return torch.cuda.current_stream().cuda_stream
 
 
+def _on_current_device(*named) -> None:
+    """The library launches on the current device with its current stream, so
+    every tensor of a call must live there (a pointer into another GPU's memory
+    would reach the kernel as a foreign address)."""
+    cur = torch.cuda.current_device()
+    for name, t in named:
+        if t.device.index != cur:
+            raise ValueError(f"{name} is on {t.device}, but the current device is cuda:{cur}")
+
+
 def _need_cuda(t: torch.Tensor, name: str, dtype=None) -> None:
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
@@ -94,8 +104,12 @@ class Workspace:
 
     def __init__(self, max_M: int, K: int, N: int, group: int, device=None):
         dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        if dev.type != "cuda":
+            raise ValueError("a workspace lives on a CUDA device")
+        if dev.index is None:
+            dev = torch.device("cuda", torch.cuda.current_device())
         self.nbytes = _binding.workspace_bytes(max(max_M, 1), K, N, K if group == -1 else group,
-                                               dev.index or 0)
+                                               dev.index)
         self.buf = torch.zeros(self.nbytes, dtype=torch.uint8, device=dev)
 
     @property
@@ -112,6 +126,7 @@ def gemm_into(x: torch.Tensor, w: PackedWeights, ws: Workspace, y: torch.Tensor,
     M, K = x.shape
     if K != w.K or tuple(y.shape) != (M, w.N):
         raise ValueError("shape mismatch")
+    _on_current_device(("x", x), ("weights", w.buf), ("workspace", ws.buf), ("y", y))
     if kernel == "auto":
         rc = _binding.gemm_raw(x.data_ptr(), w.codes_ptr, w.scales_ptr, w.zeros_ptr, y.data_ptr(), M, K,
                                w.N, w.group, ws.ptr, ws.nbytes, _stream())
@@ -143,6 +158,7 @@ def gemm_host(x_host: torch.Tensor, x_dev: torch.Tensor, w: PackedWeights, ws: W
     if (K != w.K or tuple(x_dev.shape) != (M, K) or tuple(y_dev.shape) != (M, w.N)
             or tuple(y_host.shape) != (M, w.N)):
         raise ValueError("shape mismatch")
+    _on_current_device(("x_dev", x_dev), ("weights", w.buf), ("workspace", ws.buf), ("y_dev", y_dev))
     rc = _binding.gemm_host_raw(x_host.data_ptr(), x_dev.data_ptr(), w.codes_ptr, w.scales_ptr,
                                 w.zeros_ptr, y_dev.data_ptr(), y_host.data_ptr(), M, K, w.N, w.group,
                                 ws.ptr, ws.nbytes, _stream())
@@ -221,6 +237,7 @@ def sparse_gemm_into(x: torch.Tensor, w: SparsePackedWeights, ws: Workspace, y: 
     M, K = x.shape
     if K != w.K or tuple(y.shape) != (M, w.N):
         raise ValueError("shape mismatch")
+    _on_current_device(("x", x), ("weights", w.buf), ("workspace", ws.buf), ("y", y))
     rc = _binding.sparse_gemm_raw(x.data_ptr(), w.codes_ptr, w.meta_ptr, w.scales_ptr, w.zeros_ptr,
                                   y.data_ptr(), M, K, w.N, w.group, ws.ptr, ws.nbytes, _stream())
     if rc != _binding.OK:

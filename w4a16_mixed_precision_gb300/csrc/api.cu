@@ -58,13 +58,19 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// group -1 means K; otherwise a positive multiple of 128 dividing K.
-bool normalise_group(int K, int* group) {
-  if (*group == -1) *group = K;
-  return *group > 0 && *group % 128 == 0 && K % *group == 0;
-}
-
 bool valid_shape(int K, int N) { return K > 0 && N > 0 && K % 128 == 0 && N % 128 == 0; }
+
+// Shape and group check shared by every entry point.  group -1 means K.  A
+// group that divides K but is not a multiple of 128 (32, 64: sizes some
+// quantisers produce, which the pages say "may not run") is a valid request
+// this library does not serve: MARLIN_ERR_UNSUPPORTED.  Anything else that is
+// not a positive divisor of K, or a bad shape: MARLIN_ERR_INVALID_ARG.
+marlin_status_t check_shape_group(int K, int N, int* group) {
+  if (!valid_shape(K, N)) return MARLIN_ERR_INVALID_ARG;
+  if (*group == -1) *group = K;
+  if (*group <= 0 || K % *group != 0) return MARLIN_ERR_INVALID_ARG;
+  return *group % 128 == 0 ? MARLIN_OK : MARLIN_ERR_UNSUPPORTED;
+}
 
 // Largest M served by the small-batch kernel (mma.sync path); larger M uses the
 // tcgen05 kernel.  W4A16_SMALL_M_MAX overrides it (0 disables the small path).
@@ -77,6 +83,19 @@ int small_m_max() {
     const char* e = getenv("W4A16_SMALL_M_MAX");
     int x = e ? atoi(e) : 24;
     return x < 0 ? 0 : (x > kMaxWarpM ? kMaxWarpM : x);
+  }();
+  return v;
+}
+
+// Whether the kernels read the first ring of weights before waiting for the
+// previous kernel in the stream (programmatic dependent launch).  The weights
+// are then treated as constant: they must not be written by a kernel that is
+// still running when the multiply is enqueued.  W4A16_EARLY_WEIGHTS=0 turns
+// it off.
+bool early_weights() {
+  static bool v = [] {
+    const char* e = getenv("W4A16_EARLY_WEIGHTS");
+    return !(e && atoi(e) == 0);
   }();
   return v;
 }
@@ -164,7 +183,9 @@ GemmPlan make_plan(int M, int K, int N, int group, int sms, int smem_optin, bool
   // workspace: [status 256 B][counters][partials]
   g.ws_counters_off = 256;
   g.ws_partials_off = round_up(g.ws_counters_off + sizeof(int) * (size_t)g.m_tiles * g.n_tiles, 256);
-  g.ws_bytes = g.ws_partials_off + (size_t)sms * 2 * g.bn * kTileN * sizeof(float);
+  // one fp32 partial tile (bn x 128) per CTA: a CTA publishes at most one
+  // (from its first segment); sized for #SMs CTAs, the most any plan launches
+  g.ws_bytes = g.ws_partials_off + (size_t)sms * g.bn * kTileN * sizeof(float);
   return g;
 }
 
@@ -180,7 +201,8 @@ marlin_status_t run_gemm(const uint16_t* X, const void* packed, const void* meta
                          int N, int group, void* workspace, size_t workspace_bytes, int kernel,
                          marlin_stream_t stream) {
   const bool sparse = meta != nullptr;
-  if (M < 0 || !valid_shape(K, N) || !normalise_group(K, &group)) return MARLIN_ERR_INVALID_ARG;
+  if (M < 0) return MARLIN_ERR_INVALID_ARG;
+  if (const marlin_status_t c = check_shape_group(K, N, &group)) return c;
   if (sparse) kernel = MARLIN_KERNEL_WARP;
   if (kernel == MARLIN_KERNEL_WARP && M > kMaxWarpM) return MARLIN_ERR_UNSUPPORTED;
   if (M == 0) return MARLIN_OK;
@@ -272,6 +294,7 @@ marlin_status_t run_gemm(const uint16_t* X, const void* packed, const void* meta
   p.units_per_group = g.upg;
   p.off_xchg = g.off_xchg;
   p.timeout_ns = kDefaultTimeoutNs;
+  p.early_weights = early_weights() ? 1 : 0;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t e = g.kind == kKernelSmallM
                             ? launch_small_m(x_map, p, g.grid, g.smem_bytes, sparse, st)
@@ -281,6 +304,24 @@ marlin_status_t run_gemm(const uint16_t* X, const void* packed, const void* meta
 }
 
 }  // namespace
+
+namespace w4a16 {
+
+// Workspace bytes of the plan marlin_gemm (automatic kernel choice) uses for
+// this call on the current device; a marlin_status_t value.
+int call_workspace_bytes(int M, int K, int N, int group, bool has_zeros, size_t* bytes) {
+  if (!bytes || M < 0) return MARLIN_ERR_INVALID_ARG;
+  if (const marlin_status_t c = check_shape_group(K, N, &group)) return c;
+  int dev;
+  marlin_status_t s = current_device(&dev);
+  if (s != MARLIN_OK) return s;
+  DeviceState* d;
+  if ((s = device_state(dev, &d)) != MARLIN_OK) return s;
+  *bytes = make_plan(M > 0 ? M : 1, K, N, group, d->sms, d->smem_optin, has_zeros).ws_bytes;
+  return MARLIN_OK;
+}
+
+}  // namespace w4a16
 
 extern "C" {
 
@@ -299,7 +340,7 @@ const char* marlin_status_string(marlin_status_t s) {
 
 marlin_status_t marlin_packed_layout(int K, int N, int group, int has_zeros, size_t* bytes,
                                      size_t* off_scales, size_t* off_zeros) {
-  if (!valid_shape(K, N) || !normalise_group(K, &group)) return MARLIN_ERR_INVALID_ARG;
+  if (const marlin_status_t c = check_shape_group(K, N, &group)) return c;
   const size_t G = (size_t)(K / group);
   const size_t codes = (size_t)K * N / 2;
   const size_t sc = round_up(codes, 256);
@@ -314,7 +355,7 @@ marlin_status_t marlin_packed_layout(int K, int N, int group, int has_zeros, siz
 marlin_status_t marlin_repack(const int32_t* q, const uint16_t* scales, const int32_t* zeros, int K,
                               int N, int group, void* out, marlin_stream_t stream) {
   if (!q || !scales || !out) return MARLIN_ERR_INVALID_ARG;
-  if (!valid_shape(K, N) || !normalise_group(K, &group)) return MARLIN_ERR_INVALID_ARG;
+  if (const marlin_status_t c = check_shape_group(K, N, &group)) return c;
   if (!aligned16(q) || !aligned16(scales) || !aligned16(out) || (zeros && !aligned16(zeros)))
     return MARLIN_ERR_MISALIGNED;
   size_t bytes, off_s, off_z;
@@ -333,8 +374,8 @@ marlin_status_t marlin_repack(const int32_t* q, const uint16_t* scales, const in
 }
 
 marlin_status_t marlin_workspace_bytes(int M, int K, int N, int group, int device, size_t* bytes) {
-  if (!bytes || M < 0 || !valid_shape(K, N) || !normalise_group(K, &group))
-    return MARLIN_ERR_INVALID_ARG;
+  if (!bytes || M < 0) return MARLIN_ERR_INVALID_ARG;
+  if (const marlin_status_t c = check_shape_group(K, N, &group)) return c;
   DeviceState* d;
   marlin_status_t s = device_state(device, &d);
   if (s != MARLIN_OK) return s;
@@ -370,7 +411,8 @@ marlin_status_t marlin_gemm_host(const uint16_t* X_host, uint16_t* X_dev, const 
                                  const uint16_t* scales, const int32_t* zeros, uint16_t* Y_dev,
                                  uint16_t* Y_host, int M, int K, int N, int group,
                                  void* workspace, size_t workspace_bytes, marlin_stream_t stream) {
-  if (M < 0 || !valid_shape(K, N) || !normalise_group(K, &group)) return MARLIN_ERR_INVALID_ARG;
+  if (M < 0) return MARLIN_ERR_INVALID_ARG;
+  if (const marlin_status_t c = check_shape_group(K, N, &group)) return c;
   if (M == 0) return MARLIN_OK;
   if (!X_host || !Y_host || !X_dev || !Y_dev || !packed || !scales || !workspace)
     return MARLIN_ERR_INVALID_ARG;
@@ -401,7 +443,7 @@ marlin_status_t marlin_gemm_host(const uint16_t* X_host, uint16_t* X_dev, const 
 
 marlin_status_t marlin_sparse_packed_layout(int K, int N, int group, int has_zeros, size_t* bytes,
                                             size_t* off_meta, size_t* off_scales, size_t* off_zeros) {
-  if (!valid_shape(K, N) || !normalise_group(K, &group)) return MARLIN_ERR_INVALID_ARG;
+  if (const marlin_status_t c = check_shape_group(K, N, &group)) return c;
   const size_t G = (size_t)(K / group);
   const size_t codes = (size_t)K * N / 4;
   const size_t me = round_up(codes, 256);
@@ -419,7 +461,7 @@ marlin_status_t marlin_sparse_repack(const int32_t* q, const uint16_t* scales, c
                                      int K, int N, int group, void* out, int* bad_groups,
                                      marlin_stream_t stream) {
   if (!q || !scales || !out) return MARLIN_ERR_INVALID_ARG;
-  if (!valid_shape(K, N) || !normalise_group(K, &group)) return MARLIN_ERR_INVALID_ARG;
+  if (const marlin_status_t c = check_shape_group(K, N, &group)) return c;
   if (!aligned16(q) || !aligned16(scales) || !aligned16(out) || (zeros && !aligned16(zeros)) ||
       (reinterpret_cast<uintptr_t>(bad_groups) & 3u))
     return MARLIN_ERR_MISALIGNED;

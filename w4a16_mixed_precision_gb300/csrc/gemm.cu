@@ -118,11 +118,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = ctrl->tmem_base;
   // Programmatic dependent launch: the next kernel in the stream may be
-  // scheduled as soon as SMs free up, and this one waits here, after its
-  // prologue, until the previous kernel has finished and its writes are
-  // visible -- so launch latency and set-up overlap the previous kernel.
+  // scheduled as soon as SMs free up, and this one waits, after its prologue,
+  // until the previous kernel has finished and its writes are visible -- so
+  // launch latency and set-up overlap the previous kernel.  The weights are
+  // constant inputs: with early_weights the weight producer fills the ring
+  // with them before that wait; X, Y and the workspace are touched only after.
   if (threadIdx.x == 0) griddep_launch_dependents();
-  griddep_wait();
+  if (warp != 0 || !p.early_weights) griddep_wait();
 
   if (warp == 0) {
     // ================= weights producer: codes, scales, zeros =================
@@ -138,7 +140,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = ku / units_per_group, ku_in_g = ku - g * units_per_group;
       int s = 0, issued = 0;
       uint32_t ph = 0;
+      // the first S stages need no wait; the dependency wait comes before the
+      // first bounded wait (which would otherwise time the previous kernel)
+      bool dep = !p.early_weights;
       for (int u = u_begin; u < u_end; ++u) {
+        if (!dep && issued == S) { griddep_wait(); dep = true; }
         if (!wait_thread(bar(ctrl->empty[s]), ph ^ 1u, wc)) break;
         const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
         const uint32_t fb = bar(ctrl->full[s]);
@@ -156,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++nt == p.n_tiles) { nt = 0; ++mt; }
         }
       }
+      if (!dep) griddep_wait();
       // Wait for every copy still in flight before the CTA may exit.
       const int first = issued > S ? issued - S : 0;
       for (int i = first; i < issued; ++i)
@@ -271,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kFirstDqWarp) {
     // ================= dequantisation + epilogue (16 warps) =================
-    const int dq = warp - kFirstDqWarp;       // 0..11
+    const int dq = warp - kFirstDqWarp;       // 0..15
     const int wg = dq >> 2;                   // warpgroup: takes every fourth unit
     const int quarter = warp & 3;             // TMEM lane quarter this warp may touch
     const int row = quarter * 32 + lane;      // epilogue: output column within the tile

@@ -33,7 +33,7 @@ struct GemmParams {
   const uint16_t* scales;   // fp16, tile-major [N/128][G][128]
   const uint8_t* zeros;     // zeros, tile-major bytes [N/128][G][64], or nullptr
   uint16_t* Y;              // fp16 [M][N]
-  float* partials;          // [grid][2][bn][128] fp32
+  float* partials;          // [grid][bn][128] fp32: one partial tile per CTA
   int* counters;            // [m_tiles * n_tiles]
   int* status;              // status word
   int M, K, N, group, G;
@@ -59,6 +59,7 @@ struct GemmParams {
   uint32_t off_xchg;        // small-M kernel: exchange buffer, bytes after stage 0
   int a_slots;              // tcgen05 kernel: A slots in TMEM (even, >= 4, <= kAStages)
   uint32_t a_base;          // tcgen05 kernel: TMEM column of A slot 0 (accumulators below it)
+  int early_weights;        // stream the first ring of weights before the dependency wait
   unsigned long long timeout_ns;
 };
 
@@ -80,6 +81,11 @@ cudaError_t gemm_set_smem_limit(int bytes);
 cudaError_t launch_small_m(const CUtensorMap& x_map, const GemmParams& p, int grid,
                            uint32_t smem_bytes, bool sparse, cudaStream_t stream);
 cudaError_t small_m_set_smem_limit(int bytes);
+
+// Workspace bytes of the plan marlin_gemm uses for this call on the current
+// device (not the worst case over kernels and smaller M that
+// marlin_workspace_bytes reports); returns a marlin_status_t value.
+int call_workspace_bytes(int M, int K, int N, int group, bool has_zeros, size_t* bytes);
 
 cudaError_t launch_repack(const uint32_t* q, uint32_t* out, int K, int N, cudaStream_t stream);
 // 2:4: GPTQ-order codes (+ zeros) -> kept codes and index nibbles in the sparse

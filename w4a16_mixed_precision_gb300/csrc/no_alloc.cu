@@ -8,12 +8,13 @@
 
 #include <mutex>
 
+#include "kernels.h"
 #include "marlin.h"
 
 namespace {
 
-// Maximum scratch: 8 MiB.  On a 152-SM GB300 this covers every problem whose
-// workspace fits, i.e. M up to 48 tokens (marlin_workspace_bytes tells).
+// Maximum scratch: 8 MiB.  On a 152-SM GB300 this covers every problem up to
+// M = 96 tokens (one fp32 partial tile of 96 x 128 per SM, plus counters).
 constexpr size_t kScratchBytes = (size_t)8 << 20;
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
@@ -51,8 +52,10 @@ extern "C" marlin_status_t marlin_gemm_no_alloc(const uint16_t* X, const void* p
     return MARLIN_ERR_MISALIGNED;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MARLIN_ERR_CUDA;
+  // the scratch this very call uses (its kernel and M), not the worst case
   size_t need = 0;
-  marlin_status_t s = marlin_workspace_bytes(M, K, N, group, dev, &need);
+  marlin_status_t s = static_cast<marlin_status_t>(
+      w4a16::call_workspace_bytes(M, K, N, group, zeros != nullptr, &need));
   if (s != MARLIN_OK) return s;
   if (need > kScratchBytes) return MARLIN_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;
@@ -61,7 +64,7 @@ extern "C" marlin_status_t marlin_gemm_no_alloc(const uint16_t* X, const void* p
   // must start at zero: the status word, the tile arrival counters, and the
   // partial-tile words (a zero word means "not yet written").  A completed call
   // leaves them zeroed, but one whose kernel gave up on a bounded wait may not,
-  // and this entry point does not report that; so clear the whole region.
+  // and this entry point does not report that; so clear this call's region.
   if (cudaMemsetAsync(scratch, 0, need, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MARLIN_ERR_CUDA;
   return marlin_gemm(X, packed, scales, zeros, Y, M, K, N, group, scratch, kScratchBytes, stream);

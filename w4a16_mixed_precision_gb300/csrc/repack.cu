@@ -1,8 +1,9 @@
 // repack.cu -- offline rewrite of GPTQ-order 4-bit codes, scales and zeros into
-// the layouts the fused kernels stream, dense and 2:4-sparse ("Marlin / GPTQ-Marlin", section "Tiled
-// layout et repacking": done once at load time; "Marlin Project Overview",
-// section "Key Techniques", item "Reshuffling for Access Patterns": weights and scales rearranged
-// offline into tensor-core operand order).
+// the layouts the fused kernels stream, dense and 2:4-sparse ("Marlin /
+// GPTQ-Marlin", section "Tiled layout et repacking"; "Marlin Project
+// Overview", section "Key Techniques", item "Reshuffling for Access
+// Patterns").  It runs once per weight, at load time.  The codes are laid out
+// per lane fragment, so that one 16-byte shared load per lane feeds the MMA.
 //
 // Code layout: for every 128-column tile nt and 64-row block kb, one 4 KB chunk
 // of 32-bit words [g = 0..7][l = 0..31][j = 0..3].  Word (g, l, j) carries the
@@ -22,6 +23,13 @@
 namespace w4a16 {
 
 namespace {
+
+// The multiply kernels may start reading the weights before their dependency
+// wait (they treat the weights as constant), which a kernel that simply ends
+// does not order against its own last stores.  Every repack thread therefore
+// makes its stores visible device-wide before it exits, so a multiply enqueued
+// right after a repack on the same stream reads the finished layout.
+__device__ __forceinline__ void publish_before_exit() { __threadfence(); }
 
 __global__ void repack_codes_kernel(const uint32_t* __restrict__ q, uint32_t* __restrict__ out, int K,
                                     int N, long long total) {
@@ -48,6 +56,7 @@ __global__ void repack_codes_kernel(const uint32_t* __restrict__ q, uint32_t* __
     w |= ((a >> 12) & 0xFu) << 24 | ((b >> 12) & 0xFu) << 28; // p6, p7: row +3
     out[t] = w;
   }
+  publish_before_exit();
 }
 
 // Rows of `row_vec` 16-byte vectors: src [G][NT][row] -> dst [NT][G][row].
@@ -62,6 +71,7 @@ __global__ void tile_major_kernel(const uint4* __restrict__ src, uint4* __restri
     const int gi = (int)(r / NT);
     dst[((long long)nt * G + gi) * row_vec + v] = src[t];
   }
+  publish_before_exit();
 }
 
 // ---- 2:4 sparsity ("Marlin", section "支持 2:4 稀疏加速": two of every four
@@ -135,6 +145,7 @@ __global__ void sparse_codes_kernel(const uint32_t* __restrict__ q, const uint32
     }
     out[t] = w;
   }
+  publish_before_exit();
 }
 
 __global__ void sparse_meta_kernel(const uint32_t* __restrict__ q, const uint32_t* __restrict__ zeros,
@@ -166,6 +177,7 @@ __global__ void sparse_meta_kernel(const uint32_t* __restrict__ q, const uint32_
     out[t] = w;
     if (bad && nbad) atomicAdd(bad, nbad);
   }
+  publish_before_exit();
 }
 
 int grid_for(long long work, int threads) {

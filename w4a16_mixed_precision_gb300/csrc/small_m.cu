@@ -143,11 +143,15 @@ __global__ void __launch_bounds__(kSmThreads, 1)
   __syncthreads();
   const WaitCtx wc{&ctrl->abort, p.status, p.timeout_ns};
   // Programmatic dependent launch: the next kernel in the stream may be
-  // scheduled as soon as SMs free up, and this one waits here, after its
-  // prologue, until the previous kernel has finished and its writes are
-  // visible -- so launch latency and set-up overlap the previous kernel.
+  // scheduled as soon as SMs free up, and this one waits, after its prologue,
+  // until the previous kernel has finished and its writes are visible -- so
+  // launch latency and set-up overlap the previous kernel.  The weights
+  // (codes, index nibbles, scales, zeros) are constant inputs: with
+  // early_weights the weight producer fills the ring with them before that
+  // wait, so the previous kernel's tail overlaps this one's first HBM reads.
+  // X, Y and the workspace are touched only after the wait.
   if (threadIdx.x == 0) griddep_launch_dependents();
-  griddep_wait();
+  if (warp != 0 || !p.early_weights) griddep_wait();
 
   if (warp == 0) {
     // ================= weights producer =================
@@ -167,7 +171,11 @@ __global__ void __launch_bounds__(kSmThreads, 1)
       int g = (ku / upg) * p.n_g, ku_in_g = ku - (ku / upg) * upg;
       int s = 0, issued = 0;
       uint32_t ph = 0;
+      // the first S stages need no wait; the dependency wait comes before the
+      // first bounded wait (which would otherwise time the previous kernel)
+      bool dep = !p.early_weights;
       for (int u = u_begin; u < u_end; ++u) {
+        if (!dep && issued == S) { griddep_wait(); dep = true; }
         if (!wait_thread(bar(ctrl->empty[s]), ph ^ 1u, wc)) break;
         const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
         const uint32_t fb = bar(ctrl->full[s]);
@@ -183,6 +191,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         if (++ku_in_g == upg) { ku_in_g = 0; g += p.n_g; }
         if (++ku == KT) { ku = 0; g = 0; ku_in_g = 0; ++nt; }
       }
+      if (!dep) griddep_wait();
       const int first = issued > S ? issued - S : 0;
       for (int i = first; i < issued; ++i)
         wait_drain(bar(ctrl->full[i % S]), (uint32_t)((i / S) & 1), wc);
