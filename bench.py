@@ -100,6 +100,44 @@ def recorded_traffic(workload: str):
     return e.get("dram_bytes_per_launch")
 
 
+# ---- workload description (shared by both arms) ------------------------------------
+
+def weight_bytes(K: int, N: int, g: int, asym: bool, sparse: bool) -> int:
+    codes = K * N // 4 + K * N // 8 if sparse else K * N // 2
+    return codes + (K // g) * N * 2 + ((K // g) * N // 2 if asym else 0)
+
+
+def rotation(problems):
+    """Weight rotation of a workload: per layer (K, N, group, asym), how many
+    calls of a step use it, the number P of graph phases (steps between two
+    reads of one weight copy) and the number of copies per layer, so that P
+    steps stream more than two L2s and each per-problem table rotates through
+    more than two L2s."""
+    sparse = any(p.sparse for p in problems)
+    layers = sorted({(p.K, p.N, p.group, p.asym) for p in problems})
+    uses = {lk: sum(1 for p in problems if (p.K, p.N, p.group, p.asym) == lk) for lk in layers}
+    step_wbytes = sum(weight_bytes(*lk, sparse) * uses[lk] for lk in layers)
+    P = max(1, -(-2 * L2_BYTES // step_wbytes))
+    copies = {lk: max(uses[lk] * P, -(-2 * L2_BYTES // weight_bytes(*lk, sparse)) + 1) for lk in layers}
+    return layers, uses, P, copies
+
+
+def workload_config(workload: str, problems) -> dict:
+    """The `config` object of the JSON line: the same for the GPU arm and the
+    reference arm (it depends on the workload only)."""
+    sparse = any(p.sparse for p in problems)
+    layers, uses, P, copies = rotation(problems)
+    weight_copies_bytes = sum(weight_bytes(*lk, sparse) * copies[lk] for lk in layers)
+    return {"workload": WORKLOAD_NAMES.get(workload, workload),
+            "problems_per_step": len(problems), "graph_phases": P,
+            "l2": f"inputs larger than L2: rotating weight copies ({weight_copies_bytes / 1e6:.0f} MB "
+                  f"in all), each read once per {P} step(s), so no call finds its weights in L2",
+            "timing": "step captured as a CUDA graph (one per rotation phase), replayed K times; "
+                      "CUDA events on the replay stream",
+            "step_bytes": sum(p.algorithmic_bytes() for p in problems),
+            "step_flops": sum(p.flops() for p in problems)}
+
+
 # ---- clocks --------------------------------------------------------------------
 
 class ClockSampler:
@@ -313,7 +351,7 @@ def run_reference(args, problems, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_s / max(args.steps, 1) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD_NAMES.get(args.workload, args.workload)},
+            "config": workload_config(args.workload, problems),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -324,8 +362,6 @@ def run_reference(args, problems, rank, world):
 
 def run_gpu(args, problems, rank, world, local):
     import torch
-
-    import dataclasses
 
     import w4a16_mixed_precision_gb300 as w4
     from w4a16_mixed_precision_gb300 import build as cuda_build
@@ -339,40 +375,8 @@ def run_gpu(args, problems, rank, world, local):
     peaks = load_peaks()
 
     # ---- weights: rotating copies so that no call finds its weights in L2 ----
-    # Each layer gets uses_per_step * P copies and every copy is read once per P
-    # steps, P chosen so that P steps stream more than two L2s of weights.
-    layers = sorted({(p.K, p.N, p.group, p.asym) for p in problems})
-
-    def wbytes(K, N, g, a):
-        codes = K * N // 4 + K * N // 8 if sparse else K * N // 2
-        return codes + (K // g) * N * 2 + ((K // g) * N // 2 if a else 0)
-
-    uses = {lk: sum(1 for p in problems if (p.K, p.N, p.group, p.asym) == lk) for lk in layers}
-    step_wbytes = sum(wbytes(*lk) * uses[lk] for lk in layers)
-    P = max(1, -(-2 * L2_BYTES // step_wbytes))
-    packed = {}
-    dense_pw = {}
-    for (K, N, g, a) in layers:
-        gen = make_sparse_weights if sparse else make_weights
-        Qp, S, Zp = gen(K, N, g, a, seed=seed_for(f"w:{K}:{N}:{g}:{int(a)}"))
-        tq, ts = torch.from_numpy(Qp).to(dev), torch.from_numpy(S).to(dev)
-        tz = torch.from_numpy(Zp).to(dev) if a else None
-        pw = w4.sparse_repack(tq, ts, tz, g) if sparse else w4.repack(tq, ts, tz, g)
-        if sparse and not args.no_table:
-            # the same weights in the dense layout, for the per-run comparison
-            dense_pw[(K, N, g, a)] = w4.repack(tq, ts, tz, g)
-        copies = [pw]
-        # the graphs use uses*P copies; the per-run table rotates through enough
-        # copies of this one layer to stream more than two L2s between reuses
-        n_copies = max(uses[(K, N, g, a)] * P, -(-2 * L2_BYTES // wbytes(K, N, g, a)) + 1)
-        for _ in range(n_copies - 1):
-            copies.append(dataclasses.replace(pw, buf=pw.buf.clone()))
-        packed[(K, N, g, a)] = copies
-        if sparse and not args.no_table:
-            dense_pw[(K, N, g, a)] = [dense_pw[(K, N, g, a)]] + [
-                dataclasses.replace(dense_pw[(K, N, g, a)], buf=dense_pw[(K, N, g, a)].buf.clone())
-                for _ in range(max(1, -(-2 * L2_BYTES // (K * N // 2))) )]
-    weight_copies_bytes = sum(wbytes(*lk) * len(packed[lk]) for lk in layers)
+    layers, uses, P, _ = rotation(problems)
+    packed, dense_pw, _ = make_weight_copies(problems, dev, with_dense=sparse and not args.no_table)
     max_m = max(p.M for p in problems)
     ws = {lk: w4.Workspace(max_m, lk[0], lk[1], lk[2]) for lk in layers}
     xs = [torch.from_numpy(make_activations(p.M, p.K, seed_for(p.key))).to(dev) for p in problems]
@@ -462,13 +466,7 @@ def run_gpu(args, problems, rank, world, local):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": WORKLOAD_NAMES.get(args.workload, args.workload),
-                   "problems_per_step": launches, "graph_phases": P,
-                   "l2": f"inputs larger than L2: rotating weight copies ({weight_copies_bytes / 1e6:.0f} MB "
-                         f"in all), each read once per {P} step(s), so no call finds its weights in L2",
-                   "timing": "step captured as a CUDA graph (one per rotation phase), replayed K times; "
-                             "CUDA events on the replay stream",
-                   "step_bytes": step_bytes, "step_flops": step_flops},
+        "config": workload_config(args.workload, problems),
         "gpu_launches": launches * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(args.workload),
@@ -480,6 +478,12 @@ def run_gpu(args, problems, rank, world, local):
         "e2e": e2e,
         "runs": runs,
     }
+    if not args.no_per_config and not args.shape and world == 1:
+        # release this workload's weights first: the other workloads need room
+        del graphs, packed, dense_pw, xs, ys, ws
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        line["per_config"] = per_config_tables(args.workload, dev, peaks)
     if args.workload == "prefill":
         # the timed region replays the step for seconds under the power cap:
         # the sustained (seconds-long) dense rate is the denominator
@@ -498,6 +502,81 @@ def run_gpu(args, problems, rank, world, local):
                                 "sample": desc, "seconds": s}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def make_weight_copies(problems, dev, with_dense=False):
+    """Repacked weights of every layer of a workload, as rotating copies (the
+    counts of `rotation`); with_dense: also the dense layout of 2:4 weights,
+    for the per-problem comparison.  Returns (packed, dense, bytes of copies)."""
+    import dataclasses
+
+    import torch
+
+    import w4a16_mixed_precision_gb300 as w4
+    sparse = any(p.sparse for p in problems)
+    layers, uses, P, ncopies = rotation(problems)
+    packed, dense_pw = {}, {}
+    for (K, N, g, a) in layers:
+        gen = make_sparse_weights if sparse else make_weights
+        Qp, S, Zp = gen(K, N, g, a, seed=seed_for(f"w:{K}:{N}:{g}:{int(a)}"))
+        tq, ts = torch.from_numpy(Qp).to(dev), torch.from_numpy(S).to(dev)
+        tz = torch.from_numpy(Zp).to(dev) if a else None
+        pw = w4.sparse_repack(tq, ts, tz, g) if sparse else w4.repack(tq, ts, tz, g)
+        packed[(K, N, g, a)] = [pw] + [dataclasses.replace(pw, buf=pw.buf.clone())
+                                      for _ in range(ncopies[(K, N, g, a)] - 1)]
+        if with_dense:
+            d = w4.repack(tq, ts, tz, g)
+            dense_pw[(K, N, g, a)] = [d] + [dataclasses.replace(d, buf=d.buf.clone())
+                                           for _ in range(max(1, -(-2 * L2_BYTES // (K * N // 2))))]
+        del tq, ts, tz
+    total = sum(weight_bytes(*lk, sparse) * len(packed[lk]) for lk in layers)
+    return packed, dense_pw, total
+
+
+def per_config_tables(main_workload: str, dev, peaks) -> dict:
+    """The other benchmark workloads, per problem (µs, GB/s, TFLOP/s, roofline
+    fraction, cuBLAS fp16 speedup) and summed: measured the same way as the
+    per-run table of the main workload, outside its timed region."""
+    import torch
+
+    import w4a16_mixed_precision_gb300 as w4
+    out = {}
+    for name in ("single", "70b-decode", "prefill", "asym-odd"):
+        if name == main_workload:
+            continue
+        problems = ALL_CONFIGS[name]
+        packed, _, _ = make_weight_copies(problems, dev)
+        max_m = max(p.M for p in problems)
+        ws = {lk: w4.Workspace(max_m, lk[0], lk[1], lk[2]) for lk in packed}
+        xs = [torch.from_numpy(make_activations(p.M, p.K, seed_for(p.key))).to(dev) for p in problems]
+        ys = [torch.empty((p.M, p.N), dtype=torch.float16, device=dev) for p in problems]
+        rows = per_run_table(problems, packed, ws, xs, ys, dev, peaks, w4.gemm_into)
+        for lk in ws:
+            assert w4.device_status(ws[lk]) == 0, "a kernel reported an expired wait"
+        tot_us = sum(r["us"] for r in rows)
+        tot_b = sum(p.algorithmic_bytes() for p in problems)
+        tot_f = sum(p.flops() for p in problems)
+        gbs = tot_b / (tot_us * 1e-6) / 1e9
+        tfl = tot_f / (tot_us * 1e-6) / 1e12
+        geo = float(np.exp(np.mean(np.log([r["speedup_vs_fp16"] for r in rows]))))
+        entry = {"workload": WORKLOAD_NAMES[name], "problems": len(problems),
+                 "sum_us": round(tot_us, 2), "GBps": round(gbs, 1), "TFLOPs": round(tfl, 2),
+                 "cublas_fp16_speedup_geomean": round(geo, 3), "runs": rows}
+        if name == "prefill":
+            entry["bound"] = "tensor"
+            entry["frac"] = round(tfl / peaks["bf16_tflops_sustained"], 4)
+            entry["peak"] = peaks["bf16_tflops_sustained"]
+            entry["peak_note"] = (f"{peaks['source']} bf16 sustained (the fp16 dense rate is the same); "
+                                  f"{tfl / peaks['bf16_tflops']:.3f} of the burst peak")
+        else:
+            entry["bound"] = "hbm"
+            entry["frac"] = round(gbs / peaks["hbm_gbs"], 4)
+            entry["peak"] = peaks["hbm_gbs"]
+        out[name] = entry
+        del packed, ws, xs, ys
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
 
 
 def per_run_table(problems, packed, ws, xs, ys, dev, peaks, call, dense_packed=None):
@@ -634,6 +713,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     ap.add_argument("--no-soak", action="store_true", help="skip the 1 s clock soak (profiling)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-problem tables of the other benchmark workloads")
     ap.add_argument("--shape", default=None,
                     help="one problem M,K,N[,group[,asym]] instead of a workload (profiling a single kernel)")
     args = ap.parse_args()
