@@ -56,7 +56,9 @@ typedef enum {
   MARLIN_ERR_MISALIGNED = 3,           /* a pointer is not 16-byte aligned        */
   MARLIN_ERR_WORKSPACE_TOO_SMALL = 4,  /* workspace smaller than required        */
   MARLIN_ERR_CUDA = 5,                 /* a CUDA runtime call or launch failed    */
-  MARLIN_ERR_TIMEOUT = 6               /* a bounded wait inside a kernel gave up  */
+  MARLIN_ERR_TIMEOUT = 6,              /* a bounded wait inside a kernel gave up  */
+  MARLIN_ERR_BOUNDS = 7                /* bounds-checked build only: a kernel
+                                          formed an address outside its buffer    */
 } marlin_status_t;
 
 /* Human-readable name of a status code (static string, never NULL).  No page
@@ -315,9 +317,13 @@ marlin_status_t marlin_sparse_gemm(const uint16_t* X, const void* packed, const 
 /*
  * No page passage: failure reporting of this library's bounded waits.
  * Synchronises `stream`, reads and clears the device status word that
- * marlin_gemm keeps in `workspace`, and returns MARLIN_OK or
+ * marlin_gemm keeps in `workspace`, and returns MARLIN_OK,
  * MARLIN_ERR_TIMEOUT (a bounded wait in a kernel expired; that call's Y is
- * not valid).  workspace: device, as passed to marlin_gemm.
+ * not valid) or, from a library built with -DMARLIN_DEBUG (which checks
+ * every address its kernels form against the extent of its buffer and skips
+ * the access instead of faulting), MARLIN_ERR_BOUNDS; the 32-bit word at byte
+ * 4 of the workspace then names the first failed check (cleared too).
+ * workspace: device, as passed to marlin_gemm.
  */
 marlin_status_t marlin_last_device_status(void* workspace, marlin_stream_t stream);
 

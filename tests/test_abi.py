@@ -38,7 +38,8 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings(lib):
     from w4a16_mixed_precision_gb300 import _binding
     for code, name in [(0, "MARLIN_OK"), (1, "MARLIN_ERR_INVALID_ARG"), (3, "MARLIN_ERR_MISALIGNED"),
-                       (4, "MARLIN_ERR_WORKSPACE_TOO_SMALL"), (6, "MARLIN_ERR_TIMEOUT")]:
+                       (4, "MARLIN_ERR_WORKSPACE_TOO_SMALL"), (6, "MARLIN_ERR_TIMEOUT"),
+                       (7, "MARLIN_ERR_BOUNDS"), (2, "MARLIN_ERR_UNSUPPORTED")]:
         assert _binding.status_string(code) == name
 
 

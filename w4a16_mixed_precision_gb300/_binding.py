@@ -12,6 +12,8 @@ import threading
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libw4a16_gb300.so")
+#: the bounds-checked build (-DMARLIN_DEBUG), built on demand by build.build(debug=True)
+DEBUG_LIB_PATH = os.path.join(_PKG, "_lib", "libw4a16_gb300_debug.so")
 
 # marlin_status_t
 OK = 0
@@ -21,6 +23,7 @@ ERR_MISALIGNED = 3
 ERR_WORKSPACE_TOO_SMALL = 4
 ERR_CUDA = 5
 ERR_TIMEOUT = 6
+ERR_BOUNDS = 7
 
 #: every symbol include/marlin.h declares
 EXPORTS = (
@@ -56,10 +59,17 @@ def load(path: str | None = None) -> ctypes.CDLL:
     with _lock:
         if _lib is not None:
             return _lib
-        p = path or LIB_PATH
-        if not os.path.exists(p):
-            raise RuntimeError(f"CUDA library not built: {p} is missing")
-        lib = ctypes.CDLL(p)
+        _lib = open_library(path or LIB_PATH)
+        return _lib
+
+
+def open_library(path: str) -> ctypes.CDLL:
+    """A separate handle on a build of the library (e.g. the bounds-checked
+    one, libw4a16_gb300_debug.so), with the C signatures declared."""
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path} is missing")
+    if True:
+        lib = ctypes.CDLL(path)
         P, I, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
         lib.marlin_status_string.argtypes = [I]
         lib.marlin_status_string.restype = ctypes.c_char_p
@@ -83,8 +93,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         for f in ("marlin_packed_layout", "marlin_repack", "marlin_workspace_bytes", "marlin_gemm",
                   "marlin_last_device_status"):
             getattr(lib, f).restype = I
-        _lib = lib
-        return lib
+    return lib
 
 
 def status_string(status: int) -> str:

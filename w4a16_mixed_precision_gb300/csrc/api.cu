@@ -295,6 +295,16 @@ marlin_status_t run_gemm(const uint16_t* X, const void* packed, const void* meta
   p.off_xchg = g.off_xchg;
   p.timeout_ns = kDefaultTimeoutNs;
   p.early_weights = early_weights() ? 1 : 0;
+  // extents for the bounds-checked build: the logical sizes of the caller's buffers
+  {
+    const size_t Gr = (size_t)(K / group);
+    p.codes_bytes = sparse ? (size_t)K * N / 4 : (size_t)K * N / 2;
+    p.meta_bytes = sparse ? (size_t)K * N / 8 : 0;
+    p.scales_bytes = Gr * N * 2;
+    p.zeros_bytes = zeros ? Gr * N / 2 : 0;
+    p.ws_bytes = workspace_bytes;
+    p.smem_bytes = g.smem_bytes;
+  }
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t e = g.kind == kKernelSmallM
                             ? launch_small_m(x_map, p, g.grid, g.smem_bytes, sparse, st)
@@ -334,6 +344,7 @@ const char* marlin_status_string(marlin_status_t s) {
     case MARLIN_ERR_WORKSPACE_TOO_SMALL: return "MARLIN_ERR_WORKSPACE_TOO_SMALL";
     case MARLIN_ERR_CUDA: return "MARLIN_ERR_CUDA";
     case MARLIN_ERR_TIMEOUT: return "MARLIN_ERR_TIMEOUT";
+    case MARLIN_ERR_BOUNDS: return "MARLIN_ERR_BOUNDS";
   }
   return "MARLIN_ERR_UNKNOWN";
 }
@@ -494,14 +505,14 @@ marlin_status_t marlin_last_device_status(void* workspace, marlin_stream_t strea
   if (!workspace) return MARLIN_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return MARLIN_ERR_CUDA;
-  int status = 0;
-  if (cudaMemcpy(&status, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+  int status[2] = {0, 0};
+  if (cudaMemcpy(status, workspace, sizeof(status), cudaMemcpyDeviceToHost) != cudaSuccess)
     return MARLIN_ERR_CUDA;
-  if (status != 0) {
-    const int zero = 0;
-    if (cudaMemcpy(workspace, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+  if (status[0] != 0) {
+    const int zero[2] = {0, 0};
+    if (cudaMemcpy(workspace, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
       return MARLIN_ERR_CUDA;
-    return MARLIN_ERR_TIMEOUT;
+    return (status[0] & kStatusBounds) ? MARLIN_ERR_BOUNDS : MARLIN_ERR_TIMEOUT;
   }
   return MARLIN_OK;
 }

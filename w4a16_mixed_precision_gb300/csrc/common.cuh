@@ -65,6 +65,37 @@ static __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, co
   }
 }
 
+// ---- bounds checks (MARLIN_DEBUG builds) --------------------------------------------
+// W4A16_IN_RANGE(status, off, len, size, site) is true when [off, off + len)
+// lies inside [0, size).  In a MARLIN_DEBUG build a failing check sets
+// kStatusBounds in the status word, records `site` in the word after it (the
+// first failure wins) and returns false, and the caller skips the access; a
+// copy that is skipped leaves its barrier incomplete, so the waits expire
+// (bounded) and the kernel returns.  Nothing traps.  In other builds the macro
+// is the constant true and its arguments are not evaluated.
+#ifdef MARLIN_DEBUG
+static __device__ __noinline__ void bounds_fail(int* status, int site) {
+  atomicCAS(status + 1, 0, site);
+  atomicOr(status, kStatusBounds);
+}
+__device__ __forceinline__ bool in_range_dbg(int* status, unsigned long long off, unsigned long long len,
+                                             unsigned long long size, int site) {
+  if (off + len <= size) return true;
+  bounds_fail(status, site);
+  return false;
+}
+#define W4A16_IN_RANGE(status, off, len, size, site)                                          \
+  ::w4a16::in_range_dbg((status), (unsigned long long)(off), (unsigned long long)(len),       \
+                        (unsigned long long)(size), (site))
+#else
+#define W4A16_IN_RANGE(status, off, len, size, site) true
+#endif
+
+// Shared-memory extent check: `addr` is a shared-window address, `raw` the
+// address of the dynamic shared memory's first byte.
+#define W4A16_SMEM_OK(p, raw, addr, len, site) \
+  W4A16_IN_RANGE((p).status, (addr) - (raw), (len), (p).smem_bytes, (site))
+
 // ---- striped partition --------------------------------------------------------
 
 // First unit of CTA c's stripe: floor(c * U / G).

@@ -149,11 +149,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
         const uint32_t fb = bar(ctrl->full[s]);
         mbar_arrive_expect_tx(fb, p.tx_w);
-        bulk_g2s(st + p.off_codes, codes + ((size_t)nt * KB + (size_t)ku * cpu) * kChunkCodeBytes,
-                 code_bytes, fb, pol_w);
+        const size_t c_off = ((size_t)nt * KB + (size_t)ku * cpu) * kChunkCodeBytes;
+        if (W4A16_IN_RANGE(p.status, c_off, code_bytes, p.codes_bytes, 21) &&
+            W4A16_SMEM_OK(p, raw_addr, st + p.off_codes, code_bytes, 24))
+          bulk_g2s(st + p.off_codes, codes + c_off, code_bytes, fb, pol_w);
         const size_t grow = (size_t)nt * p.G + g;  // tile-major group row
-        bulk_g2s(st + p.off_scales, p.scales + grow * kTileN, kTileN * 2, fb, pol_w);
-        if (p.zeros) bulk_g2s(st + p.off_zeros, p.zeros + grow * (kTileN / 2), kTileN / 2, fb, pol_w);
+        if (W4A16_IN_RANGE(p.status, grow * kTileN * 2, kTileN * 2, p.scales_bytes, 22) &&
+            W4A16_SMEM_OK(p, raw_addr, st + p.off_scales, kTileN * 2, 24))
+          bulk_g2s(st + p.off_scales, p.scales + grow * kTileN, kTileN * 2, fb, pol_w);
+        if (p.zeros && W4A16_IN_RANGE(p.status, grow * (kTileN / 2), kTileN / 2, p.zeros_bytes, 23) &&
+            W4A16_SMEM_OK(p, raw_addr, st + p.off_zeros, kTileN / 2, 24))
+          bulk_g2s(st + p.off_zeros, p.zeros + grow * (kTileN / 2), kTileN / 2, fb, pol_w);
         ++issued;
         if (++s == S) { s = 0; ph ^= 1u; }
         if (++ku_in_g == units_per_group) { ku_in_g = 0; ++g; }
@@ -184,8 +190,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(fb, p.tx_x);
         const int k0 = ku * cpu * kChunkK;
         for (int j = 0; j < cpu; ++j)
-          tma_load_2d(st + (uint32_t)j * p.x_chunk_bytes, &x_map, k0 + j * kChunkK, mt * p.bn, fb,
-                      pol_x);
+          if (W4A16_SMEM_OK(p, raw_addr, st + (uint32_t)j * p.x_chunk_bytes, p.x_chunk_bytes, 25))
+            tma_load_2d(st + (uint32_t)j * p.x_chunk_bytes, &x_map, k0 + j * kChunkK, mt * p.bn, fb,
+                        pol_x);
         ++issued;
         if (++s == S) { s = 0; ph ^= 1u; }
         if (++ku == KT) {
@@ -250,6 +257,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
           const uint32_t a_col = tmem + p.a_base + (uint32_t)a * a_cols;
+          // the accumulator columns and the A slot lie in the allocation; B
+          // (this issuer's X rows of every chunk) lies in the stage
+          if (!W4A16_IN_RANGE(p.status, (d_tmem - tmem) & 0xFFFFu, n_iss, kTmemCols, 28) ||
+              !W4A16_IN_RANGE(p.status, (a_col - tmem) & 0xFFFFu, a_cols, kTmemCols, 28) ||
+              !W4A16_SMEM_OK(p, raw_addr, st + x_rows, (uint32_t)(cpu - 1) * p.x_chunk_bytes + n_iss * 128u, 27)) {
+            ok = false;
+            break;
+          }
           for (int j = 0; j < cpu; ++j) {
             const uint64_t desc0 = umma_desc_sw128(st + (uint32_t)j * p.x_chunk_bytes + x_rows);
 #pragma unroll
@@ -315,19 +330,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_warp(bar(ctrl->full[s]), ph, wc)) { ok = false; break; }
           const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
           // a unit (cpu <= 2 chunks of 64 rows, group >= 128) lies in one group row
-          const uint4 w0 = lds128(st + code_off);        // chunk 0, group 2q
-          const uint4 w1 = lds128(st + code_off + 512);  // chunk 0, group 2q+1
+          const bool cok = W4A16_SMEM_OK(p, raw_addr, st + code_off, (cpu - 1) * kChunkCodeBytes + 512 + 16, 26);
+          const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+          const uint4 w0 = cok ? lds128(st + code_off) : z4;        // chunk 0, group 2q
+          const uint4 w1 = cok ? lds128(st + code_off + 512) : z4;  // chunk 0, group 2q+1
           uint32_t z0 = 8, z1 = 8, z2 = 8, z3 = 8;
-          if (has_zeros) {
+          if (has_zeros && W4A16_SMEM_OK(p, raw_addr, st + zr_off, 13, 26)) {
             z0 = (lds_u8(st + zr_off) >> z_shift) & 0xFu;
             z1 = (lds_u8(st + zr_off + 4) >> z_shift) & 0xFu;
             z2 = (lds_u8(st + zr_off + 8) >> z_shift) & 0xFu;
             z3 = (lds_u8(st + zr_off + 12) >> z_shift) & 0xFu;
           }
-          const ColConst k0 = col_const((uint16_t)lds_u16(st + sc_off), z0);
-          const ColConst k1 = col_const((uint16_t)lds_u16(st + sc_off + 16), z1);
-          const ColConst k2 = col_const((uint16_t)lds_u16(st + sc_off + 32), z2);
-          const ColConst k3 = col_const((uint16_t)lds_u16(st + sc_off + 48), z3);
+          const bool sok = W4A16_SMEM_OK(p, raw_addr, st + sc_off, 50, 26);
+          const ColConst k0 = col_const(sok ? (uint16_t)lds_u16(st + sc_off) : 0, z0);
+          const ColConst k1 = col_const(sok ? (uint16_t)lds_u16(st + sc_off + 16) : 0, z1);
+          const ColConst k2 = col_const(sok ? (uint16_t)lds_u16(st + sc_off + 32) : 0, z2);
+          const ColConst k3 = col_const(sok ? (uint16_t)lds_u16(st + sc_off + 48) : 0, z3);
           // the first chunk is dequantised before waiting for the slot, so that
           // only its stores sit between the slot's release and its refill
           uint32_t d0[16], d1[16];
@@ -336,11 +354,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_warp(bar(ctrl->aempty[a]), aph ^ 1u, wc)) { ok = false; break; }
           tc_fence_after();
           const uint32_t acol = tmem + p.a_base + (uint32_t)a * a_cols + lane_off;
+          // this warp's 32 lanes and the slot's a_cols columns lie in the allocation
+          if (!W4A16_IN_RANGE(p.status, (acol - tmem) & 0xFFFFu, a_cols, kTmemCols, 27) ||
+              !W4A16_IN_RANGE(p.status, ((acol - tmem) >> 16) + 32u, 0, 128, 27)) {
+            ok = false;
+            break;
+          }
           tmem_st_16x256b_x4(acol, d0);
           tmem_st_16x256b_x4(acol + (16u << 16), d1);
           if (cpu == 2) {
-            const uint4 v0 = lds128(st + code_off + kChunkCodeBytes);
-            const uint4 v1 = lds128(st + code_off + kChunkCodeBytes + 512);
+            const uint4 v0 = cok ? lds128(st + code_off + kChunkCodeBytes) : z4;
+            const uint4 v1 = cok ? lds128(st + code_off + kChunkCodeBytes + 512) : z4;
             const uint32_t c1 = acol + (uint32_t)(kChunkK / 2);
             dequant_store_tmem(c1, v0, k0.sub, k1.add, k0.s, k1.s);
             dequant_store_tmem(c1 + (16u << 16), v1, k2.sub, k3.add, k2.s, k3.s);
@@ -372,7 +396,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // of contributors, while every thread polls its own words of their
         // partial tiles (a tagged word is final once non-zero)
         if (lane == 0) {
-          if (wait_counter(&p.counters[tile], (int)(c_last - c_first), wc))
+          if (W4A16_IN_RANGE(p.status, (const char*)&p.counters[tile] - (const char*)p.status, 4, p.ws_bytes,
+                             32) &&
+              wait_counter(&p.counters[tile], (int)(c_last - c_first), wc))
             p.counters[tile] = 0;  // leave the workspace zeroed for the next call
           mbar_arrive(bar(ctrl->red_go));
         }
@@ -387,6 +413,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool got = true, go_seen = !reducer;
       for (int cc = wg; cc < p.bn / 8; cc += kNumDqWG) {
         uint32_t r[8], r1[8];
+        if (!W4A16_IN_RANGE(p.status, d_first + (uint32_t)cc * 8, 8, kTmemCols, 29) ||
+            (two && !W4A16_IN_RANGE(p.status, (uint32_t)(p.bn + cc * 8), 8, kTmemCols, 29))) {
+          got = false;
+          break;
+        }
         tmem_ld_x8(tmem + lane_off + d_first + (uint32_t)cc * 8, r);
         if (two) tmem_ld_x8(tmem + lane_off + (uint32_t)(p.bn + cc * 8), r1);
         tmem_wait_ld();
@@ -403,6 +434,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (long long q0 = c_first + 1; q0 <= c_last; q0 += 2) {
             const int nq = (int)min(2LL, c_last - q0 + 1);
             float* base = p.partials + (size_t)q0 * part_stride;
+            // the partial tiles of contributors q0 .. q0 + nq - 1 this thread polls
+            if (!W4A16_IN_RANGE(p.status, (const char*)base - (const char*)p.status,
+                                4 * (size_t)nq * part_stride, p.ws_bytes, 31)) { got = false; break; }
             uint32_t raw[16];
             if (!poll_partials<2, 8>(base, part_stride, off, nq, raw, wc)) { got = false; break; }
 #pragma unroll
@@ -428,9 +462,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 8; ++c) {
           const int m = cc * 8 + c;
           if (whole || reducer) {
-            if (m_base + m < p.M)
+            if (m_base + m < p.M &&
+                W4A16_IN_RANGE(p.status, (size_t)(m_base + m) * p.N + y_col, 1, (size_t)p.M * p.N, 30))
               p.Y[(size_t)(m_base + m) * p.N + y_col] = __half_as_ushort(__float2half_rn(acc[c]));
-          } else {
+          } else if (W4A16_IN_RANGE(p.status, (const char*)(part + (size_t)m * kTileN + row) - (const char*)p.status,
+                                    4, p.ws_bytes, 31)) {
             st_partial(part + (size_t)m * kTileN + row, acc[c]);
           }
         }
@@ -441,7 +477,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(ctrl->dempty));
       // contributor (this is its first segment): its tagged words are its
       // publication; count it in and go on without waiting
-      if (!whole && !reducer && dq == 0 && lane == 0) red_relaxed_gpu_add(&p.counters[tile], 1);
+      if (!whole && !reducer && dq == 0 && lane == 0 &&
+          W4A16_IN_RANGE(p.status, (const char*)&p.counters[tile] - (const char*)p.status, 4, p.ws_bytes, 32))
+        red_relaxed_gpu_add(&p.counters[tile], 1);
       ++seg;
       u += seg_len;
       ku = 0;

@@ -24,8 +24,10 @@ constexpr int kMaxStages = 16;
 constexpr int kCtrlBytes = 1024;   // barriers and flags at the front of dynamic smem
 constexpr int kMaxBn = 256;        // tokens per m-tile (UMMA N)
 
-// Device status word bits (workspace offset 0).
+// Device status word bits (workspace offset 0).  The word at offset 4 holds
+// the site of the first failed bounds check (debug builds only).
 constexpr int kStatusTimeout = 1;
+constexpr int kStatusBounds = 2;
 
 struct GemmParams {
   const uint32_t* codes;    // tile-layout codes
@@ -61,6 +63,11 @@ struct GemmParams {
   uint32_t a_base;          // tcgen05 kernel: TMEM column of A slot 0 (accumulators below it)
   int early_weights;        // stream the first ring of weights before the dependency wait
   unsigned long long timeout_ns;
+  // Extents the bounds-checked (MARLIN_DEBUG) build checks addresses against,
+  // in bytes: the logical sizes of the buffers the caller passed, and the
+  // dynamic shared memory of the launch.
+  unsigned long long codes_bytes, meta_bytes, scales_bytes, zeros_bytes, ws_bytes;
+  uint32_t smem_bytes;
 };
 
 // Partition and resource plan of one marlin_gemm call.

@@ -181,11 +181,19 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         const uint32_t fb = bar(ctrl->full[s]);
         mbar_arrive_expect_tx(fb, tx);
         const size_t chunk0 = (size_t)nt * KB + (size_t)ku * cpu;
-        bulk_g2s(st + p.off_codes, codes + chunk0 * chunk_code, code_bytes, fb, pol);
-        if (SP) bulk_g2s(st + p.off_meta, meta + chunk0 * kSpChunkMetaBytes, meta_bytes, fb, pol);
+        if (W4A16_IN_RANGE(p.status, chunk0 * chunk_code, code_bytes, p.codes_bytes, 1) &&
+            W4A16_SMEM_OK(p, raw_addr, st + p.off_codes, code_bytes, 5))
+          bulk_g2s(st + p.off_codes, codes + chunk0 * chunk_code, code_bytes, fb, pol);
+        if (SP && W4A16_IN_RANGE(p.status, chunk0 * kSpChunkMetaBytes, meta_bytes, p.meta_bytes, 2) &&
+            W4A16_SMEM_OK(p, raw_addr, st + p.off_meta, meta_bytes, 5))
+          bulk_g2s(st + p.off_meta, meta + chunk0 * kSpChunkMetaBytes, meta_bytes, fb, pol);
         const size_t grow = (size_t)nt * p.G + g;
-        bulk_g2s(st + p.off_scales, p.scales + grow * kTileN, scale_bytes, fb, pol);
-        if (p.zeros) bulk_g2s(st + p.off_zeros, p.zeros + grow * (kTileN / 2), zero_bytes, fb, pol);
+        if (W4A16_IN_RANGE(p.status, grow * kTileN * 2, scale_bytes, p.scales_bytes, 3) &&
+            W4A16_SMEM_OK(p, raw_addr, st + p.off_scales, scale_bytes, 5))
+          bulk_g2s(st + p.off_scales, p.scales + grow * kTileN, scale_bytes, fb, pol);
+        if (p.zeros && W4A16_IN_RANGE(p.status, grow * (kTileN / 2), zero_bytes, p.zeros_bytes, 4) &&
+            W4A16_SMEM_OK(p, raw_addr, st + p.off_zeros, zero_bytes, 5))
+          bulk_g2s(st + p.off_zeros, p.zeros + grow * (kTileN / 2), zero_bytes, fb, pol);
         ++issued;
         if (++s == S) { s = 0; ph ^= 1u; }
         if (++ku_in_g == upg) { ku_in_g = 0; g += p.n_g; }
@@ -211,7 +219,8 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         mbar_arrive_expect_tx(fb, tx);
         const int k0 = ku * cpu * kChunkK;
         for (int j = 0; j < cpu; ++j)
-          tma_load_2d(st + (uint32_t)j * p.x_chunk_bytes, &x_map, k0 + j * kChunkK, 0, fb, pol);
+          if (W4A16_SMEM_OK(p, raw_addr, st + (uint32_t)j * p.x_chunk_bytes, p.x_chunk_bytes, 6))
+            tma_load_2d(st + (uint32_t)j * p.x_chunk_bytes, &x_map, k0 + j * kChunkK, 0, fb, pol);
         ++issued;
         if (++s == S) { s = 0; ph ^= 1u; }
         if (++ku == KT) ku = 0;
@@ -292,23 +301,30 @@ __global__ void __launch_bounds__(kSmThreads, 1)
           // x, y: code words of the chunk's two steps; z, w: their index words
 #pragma unroll
           for (int jj = 0; jj < JPW; ++jj) {
-            const uint2 cw = lds64(st + code_off + (uint32_t)jj * kSpChunkCodeBytes);
-            const uint2 mw = lds64(st + meta_off + (uint32_t)jj * kSpChunkMetaBytes);
+            const uint32_t ca = st + code_off + (uint32_t)jj * kSpChunkCodeBytes;
+            const uint32_t ma = st + meta_off + (uint32_t)jj * kSpChunkMetaBytes;
+            const uint2 cw = W4A16_SMEM_OK(p, raw_addr, ca, 8, 7) ? lds64(ca) : make_uint2(0u, 0u);
+            const uint2 mw = W4A16_SMEM_OK(p, raw_addr, ma, 8, 7) ? lds64(ma) : make_uint2(0u, 0u);
             wv[jj] = make_uint4(cw.x, cw.y, mw.x, mw.y);
           }
         } else {
 #pragma unroll
-          for (int jj = 0; jj < JPW; ++jj) wv[jj] = lds128(st + code_off + (uint32_t)jj * kChunkCodeBytes);
+          for (int jj = 0; jj < JPW; ++jj) {
+            const uint32_t ca = st + code_off + (uint32_t)jj * kChunkCodeBytes;
+            wv[jj] = W4A16_SMEM_OK(p, raw_addr, ca, 16, 7) ? lds128(ca) : make_uint4(0u, 0u, 0u, 0u);
+          }
         }
         // implicit zero 8: 1024 + 8 and -(64 + 8) as fp16 pairs
         uint32_t sub0 = 0x64086408u, add1 = 0xD480D480u;
         if constexpr (ZP) {
-          const uint32_t zb0 = lds_u8(st + zr_off), zb1 = lds_u8(st + zr_off + 4);
+          const bool zok = W4A16_SMEM_OK(p, raw_addr, st + zr_off, 5, 8);
+          const uint32_t zb0 = zok ? lds_u8(st + zr_off) : 0u, zb1 = zok ? lds_u8(st + zr_off + 4) : 0u;
           const ColConst k0 = col_const(0, (zb0 >> z_shift) & 0xFu);
           const ColConst k1 = col_const(0, (zb1 >> z_shift) & 0xFu);
           sub0 = k0.sub; add1 = k1.add;
         }
-        const uint32_t sr = lds_u16(st + sc_off), sr8 = lds_u16(st + sc_off + 16);
+        const bool sok = W4A16_SMEM_OK(p, raw_addr, st + sc_off, 18, 8);
+        const uint32_t sr = sok ? lds_u16(st + sc_off) : 0u, sr8 = sok ? lds_u16(st + sc_off + 16) : 0u;
         const uint32_t s0 = sr | (sr << 16), s1 = sr8 | (sr8 << 16);
         if constexpr (SP) {
 #pragma unroll
@@ -317,7 +333,10 @@ __global__ void __launch_bounds__(kSmThreads, 1)
             for (int ks = 0; ks < 2; ++ks) {
               uint4 b[NB];
 #pragma unroll
-              for (int nb = 0; nb < NB; ++nb) b[nb] = ldmatrix_x4(st + xoff[jj][ks] + (uint32_t)nb * 1024);
+              for (int nb = 0; nb < NB; ++nb) {
+                const uint32_t xa = st + xoff[jj][ks] + (uint32_t)nb * 1024;
+                b[nb] = W4A16_SMEM_OK(p, raw_addr, xa, 16, 9) ? ldmatrix_x4(xa) : make_uint4(0u, 0u, 0u, 0u);
+              }
               const uint32_t w = ks ? wv[jj].y : wv[jj].x;
               const uint32_t e = ks ? wv[jj].w : wv[jj].z;
               if (kTwoChains && ks) dequant_mma_sp<NB>(acc2, w, e, sub0, add1, s0, s1, b);
@@ -331,7 +350,10 @@ __global__ void __launch_bounds__(kSmThreads, 1)
             for (int ks = 0; ks < 4; ++ks) {
               uint2 b[NB];
 #pragma unroll
-              for (int nb = 0; nb < NB; ++nb) b[nb] = lds64(st + xoff[jj][ks] + (uint32_t)nb * 1024);
+              for (int nb = 0; nb < NB; ++nb) {
+                const uint32_t xa = st + xoff[jj][ks] + (uint32_t)nb * 1024;
+                b[nb] = W4A16_SMEM_OK(p, raw_addr, xa, 8, 9) ? lds64(xa) : make_uint2(0u, 0u);
+              }
               if (kTwoChains && (ks & 1)) dequant_mma<NB>(acc2, wk[ks], sub0, add1, s0, s1, b);
               else dequant_mma<NB>(acc, wk[ks], sub0, add1, s0, s1, b);
             }
@@ -355,7 +377,10 @@ __global__ void __launch_bounds__(kSmThreads, 1)
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-          for (int d = 0; d < 4; ++d) xchg[(nb * 4 + d) * 256 + g * 32 + lane] = acc[nb][d];
+          for (int d = 0; d < 4; ++d) {
+            float* xp = &xchg[(nb * 4 + d) * 256 + g * 32 + lane];
+            if (W4A16_SMEM_OK(p, raw_addr, smem_addr(xp), 4, 10)) *xp = acc[nb][d];
+          }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(ctrl->red_full));
       } else {
@@ -363,7 +388,10 @@ __global__ void __launch_bounds__(kSmThreads, 1)
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-          for (int d = 0; d < 4; ++d) acc[nb][d] += xchg[(nb * 4 + d) * 256 + g * 32 + lane];
+          for (int d = 0; d < 4; ++d) {
+            const float* xp = &xchg[(nb * 4 + d) * 256 + g * 32 + lane];
+            acc[nb][d] += W4A16_SMEM_OK(p, raw_addr, smem_addr(xp), 4, 10) ? *xp : 0.f;
+          }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(ctrl->red_free));
 
@@ -376,7 +404,8 @@ __global__ void __launch_bounds__(kSmThreads, 1)
 #pragma unroll
             for (int d = 0; d < 4; ++d) {
               const int m = 8 * nb + ((d & 1) ? tok1 : tok0);
-              if (m < p.M)
+              if (m < p.M && W4A16_IN_RANGE(p.status, (size_t)m * p.N + y_col0 + 8 * (d >> 1), 1,
+                                            (size_t)p.M * p.N, 11))
                 p.Y[(size_t)m * p.N + y_col0 + 8 * (d >> 1)] =
                     __half_as_ushort(__float2half_rn(acc[nb][d]));
             }
@@ -392,9 +421,13 @@ __global__ void __launch_bounds__(kSmThreads, 1)
 #pragma unroll
               for (int d = 0; d < 4; ++d) {
                 const int m = 8 * nb + ((d & 1) ? tok1 : tok0);
-                st_partial(part + (size_t)m * kTileN + col_r + 8 * (d >> 1), acc[nb][d]);
+                float* pw = part + (size_t)m * kTileN + col_r + 8 * (d >> 1);
+                if (W4A16_IN_RANGE(p.status, (const char*)pw - (const char*)p.status, 4, p.ws_bytes, 12))
+                  st_partial(pw, acc[nb][d]);
               }
-            if (g == 0 && lane == 0) red_relaxed_gpu_add(&p.counters[tile], 1);
+            if (g == 0 && lane == 0 &&
+                W4A16_IN_RANGE(p.status, (const char*)&p.counters[tile] - (const char*)p.status, 4, p.ws_bytes, 13))
+              red_relaxed_gpu_add(&p.counters[tile], 1);
           } else {
             // reducer (this is its last segment): every thread polls its own
             // words of the other contributors' partials (a word is final once
@@ -403,7 +436,9 @@ __global__ void __launch_bounds__(kSmThreads, 1)
             // contributors before Y is written
             if (g == 0) {
               if (lane == 0) {
-                if (wait_counter(&p.counters[tile], (int)(c_last - c_first), wc))
+                if (W4A16_IN_RANGE(p.status, (const char*)&p.counters[tile] - (const char*)p.status, 4,
+                                   p.ws_bytes, 13) &&
+                    wait_counter(&p.counters[tile], (int)(c_last - c_first), wc))
                   p.counters[tile] = 0;  // leave the workspace zeroed for the next call
                 mbar_arrive(bar(ctrl->red_go));
               }
@@ -421,6 +456,9 @@ __global__ void __launch_bounds__(kSmThreads, 1)
               for (long long q0 = c_first + 1; q0 <= c_last && got; q0 += 4) {
                 const int nq = (int)min(4LL, c_last - q0 + 1);
                 float* base = p.partials + (size_t)q0 * stride;
+                // the partial tiles of contributors q0 .. q0 + nq - 1 this thread polls
+                if (!W4A16_IN_RANGE(p.status, (const char*)base - (const char*)p.status,
+                                    4 * (size_t)nq * stride, p.ws_bytes, 12)) { got = false; break; }
                 uint32_t raw[16];
                 if (!poll_partials<4, 4>(base, stride, off, nq, raw, wc)) { got = false; break; }
 #pragma unroll
@@ -441,7 +479,8 @@ __global__ void __launch_bounds__(kSmThreads, 1)
 #pragma unroll
               for (int d = 0; d < 4; ++d) {
                 const int m = 8 * nb + ((d & 1) ? tok1 : tok0);
-                if (m < p.M)
+                if (m < p.M && W4A16_IN_RANGE(p.status, (size_t)m * p.N + y_col0 + 8 * (d >> 1), 1,
+                                              (size_t)p.M * p.N, 11))
                   p.Y[(size_t)m * p.N + y_col0 + 8 * (d >> 1)] =
                       __half_as_ushort(__float2half_rn(acc[nb][d]));
               }
