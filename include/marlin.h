@@ -296,14 +296,16 @@ marlin_status_t marlin_sparse_repack(const int32_t* q, const uint16_t* scales, c
 
 /*
  * Y = X . dequant(W) for 2:4-sparse weights: dequantises only the kept half
- * of the codes and multiplies with mma.sp on the warp-level path (M <= 32).
+ * of the codes and multiplies with mma.sp on the warp-level path, in m-tiles
+ * of up to 32 tokens (every M; above 32 tokens each m-tile reads the same
+ * weights again, from L2).
  *
  * packed     device, the codes region of a marlin_sparse_repack output.
  * meta       device, the meta region (packed + off_meta); NULL -> INVALID_ARG.
  * scales     device, packed + off_scales.  zeros: packed + off_zeros or NULL.
  * X, Y, workspace, stream, determinism, errors: as for marlin_gemm; a
  * workspace sized by marlin_workspace_bytes(M, K, N, group, ...) serves this
- * call too.  M > 32 -> MARLIN_ERR_UNSUPPORTED.  Results agree with
+ * call too (it covers every M it was sized for).  Results agree with
  * marlin_gemm's on the expanded weights within the parity tolerance (the
  * fp32 summation orders differ).  Only the kept terms enter the sum, so for
  * an inf or NaN in X at a dropped row the result is not specified here (the

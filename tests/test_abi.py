@@ -130,9 +130,9 @@ def test_sparse_host_checks(lib):
     from w4a16_mixed_precision_gb300 import _binding as b
     g = 0x10000
     call = b.sparse_gemm_raw
-    # meta is required; M > 32 is not served (warp-level path only)
+    # meta is required; the dense warp-level kernel forced above 32 tokens is not served
     assert call(g, g, None, g, None, g, 4, 256, 256, 128, g, 1 << 20, 0) == b.ERR_INVALID_ARG
-    assert call(g, g, g, g, None, g, 33, 256, 256, 128, g, 1 << 20, 0) == b.ERR_UNSUPPORTED
+    assert b.gemm_ex_raw(g, g, g, None, g, 33, 256, 256, 128, g, 1 << 20, 1, 0) == b.ERR_UNSUPPORTED
     assert call(g, g, g, g, None, g, 0, 256, 256, 128, g, 1 << 20, 0) == b.OK
     assert call(g, g, g, g, None, g, 4, 256, 200, 128, g, 1 << 20, 0) == b.ERR_INVALID_ARG
     assert call(g, g, g + 8, g, None, g, 4, 256, 256, 128, g, 1 << 20, 0) == b.ERR_MISALIGNED

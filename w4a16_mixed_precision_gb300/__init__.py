@@ -231,7 +231,7 @@ def sparse_repack(q: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor | N
 
 
 def sparse_gemm_into(x: torch.Tensor, w: SparsePackedWeights, ws: Workspace, y: torch.Tensor) -> torch.Tensor:
-    """y[M, N] = x[M, K] . dequant(W) for 2:4-sparse W (M <= 32), fp16, on the current stream."""
+    """y[M, N] = x[M, K] . dequant(W) for 2:4-sparse W, fp16, on the current stream."""
     _need_cuda(x, "x", torch.float16)
     _need_cuda(y, "y", torch.float16)
     M, K = x.shape

@@ -131,13 +131,14 @@ GemmPlan make_plan(int M, int K, int N, int group, int sms, int smem_optin, bool
   const bool warp_level =
       kernel == MARLIN_KERNEL_WARP || (kernel == MARLIN_KERNEL_AUTO && M <= small_m_max());
   if (warp_level) {
-    // tokens in blocks of 8 (the mma.sync N dimension)
+    // tokens in blocks of 8 (the mma.sync N dimension), at most 32 per m-tile;
+    // larger batches (the 2:4 path only) take several m-tiles of 32
     g.kind = kKernelSmallM;
-    g.bn = 8 * ((M + 7) / 8);
+    g.bn = M <= kMaxWarpM ? 8 * ((M + 7) / 8) : kMaxWarpM;
     if (g.bn < 8) g.bn = 8;
-    g.m_tiles = 1;
+    g.m_tiles = (M + g.bn - 1) / g.bn;
     const bool can4 = K % 256 == 0 && (group == 128 || group % 256 == 0);
-    const long long units4 = (long long)g.n_tiles * (K / 256);
+    const long long units4 = (long long)g.m_tiles * g.n_tiles * (K / 256);
     g.cpu = (can4 && units4 >= 8LL * sms) ? 4 : 2;
   } else {
     g.kind = kKernelTcgen05;
@@ -203,8 +204,8 @@ marlin_status_t run_gemm(const uint16_t* X, const void* packed, const void* meta
   const bool sparse = meta != nullptr;
   if (M < 0) return MARLIN_ERR_INVALID_ARG;
   if (const marlin_status_t c = check_shape_group(K, N, &group)) return c;
+  if (!sparse && kernel == MARLIN_KERNEL_WARP && M > kMaxWarpM) return MARLIN_ERR_UNSUPPORTED;
   if (sparse) kernel = MARLIN_KERNEL_WARP;
-  if (kernel == MARLIN_KERNEL_WARP && M > kMaxWarpM) return MARLIN_ERR_UNSUPPORTED;
   if (M == 0) return MARLIN_OK;
   if (!X || !packed || !scales || !Y || !workspace) return MARLIN_ERR_INVALID_ARG;
   if (!aligned16(X) || !aligned16(packed) || !aligned16(scales) || (zeros && !aligned16(zeros)) ||
@@ -397,6 +398,11 @@ marlin_status_t marlin_workspace_bytes(int M, int K, int N, int group, int devic
   const GemmPlan w = make_plan(m < kMaxWarpM ? m : kMaxWarpM, K, N, group, d->sms, d->smem_optin, true,
                                MARLIN_KERNEL_WARP);
   if (w.ws_bytes > need) need = w.ws_bytes;
+  if (m > kMaxWarpM) {
+    // the 2:4 path at this M: m-tiles of 32 tokens, one counter per (tile, m-tile)
+    const GemmPlan sp = make_plan(m, K, N, group, d->sms, d->smem_optin, true, MARLIN_KERNEL_WARP, true);
+    if (sp.ws_bytes > need) need = sp.ws_bytes;
+  }
   *bytes = need;
   return MARLIN_OK;
 }

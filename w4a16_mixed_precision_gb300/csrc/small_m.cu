@@ -1,5 +1,6 @@
 // small_m.cu -- the fused W4A16 matrix multiply for small batches (M <= 32; by
-// default the library sends M <= 24 here and larger batches to gemm.cu):
+// default the library sends M <= 24 here and larger batches to gemm.cu; the
+// 2:4-sparse instantiation serves every M, in m-tiles of 32 tokens):
 // Y[M][N] = X[M][K] . dequant(W)[K][N] on the warp-level tensor-core path.
 //
 // At M <= 32 the multiply is bound by streaming the 4-bit weights from HBM, and
@@ -167,7 +168,10 @@ __global__ void __launch_bounds__(kSmThreads, 1)
       const uint32_t zero_bytes = (uint32_t)(p.n_g * kTileN / 2);
       const uint32_t tx = code_bytes + meta_bytes + scale_bytes + (p.zeros ? zero_bytes : 0u);
       const int upg = p.units_per_group;
-      int nt = tile_begin, ku = ku_begin;
+      // tiles are (column tile, m-tile) pairs, m-tile fastest: the m-tiles of
+      // a column tile read the same weights one after the other (from L2)
+      const int MT = p.m_tiles;
+      int nt = tile_begin / MT, mt = tile_begin - (tile_begin / MT) * MT, ku = ku_begin;
       int g = (ku / upg) * p.n_g, ku_in_g = ku - (ku / upg) * upg;
       int s = 0, issued = 0;
       uint32_t ph = 0;
@@ -197,7 +201,10 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         ++issued;
         if (++s == S) { s = 0; ph ^= 1u; }
         if (++ku_in_g == upg) { ku_in_g = 0; g += p.n_g; }
-        if (++ku == KT) { ku = 0; g = 0; ku_in_g = 0; ++nt; }
+        if (++ku == KT) {
+          ku = 0; g = 0; ku_in_g = 0;
+          if (++mt == MT) { mt = 0; ++nt; }
+        }
       }
       if (!dep) griddep_wait();
       const int first = issued > S ? issued - S : 0;
@@ -209,7 +216,8 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     if (lane == 0) {
       const uint64_t pol = policy_evict_last();
       const uint32_t tx = (uint32_t)cpu * p.x_chunk_bytes;
-      int ku = ku_begin;
+      const int MT = p.m_tiles;
+      int mt = tile_begin - (tile_begin / MT) * MT, ku = ku_begin;
       int s = 0, issued = 0;
       uint32_t ph = 0;
       for (int u = u_begin; u < u_end; ++u) {
@@ -220,10 +228,13 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         const int k0 = ku * cpu * kChunkK;
         for (int j = 0; j < cpu; ++j)
           if (W4A16_SMEM_OK(p, raw_addr, st + (uint32_t)j * p.x_chunk_bytes, p.x_chunk_bytes, 6))
-            tma_load_2d(st + (uint32_t)j * p.x_chunk_bytes, &x_map, k0 + j * kChunkK, 0, fb, pol);
+            tma_load_2d(st + (uint32_t)j * p.x_chunk_bytes, &x_map, k0 + j * kChunkK, mt * p.bn, fb, pol);
         ++issued;
         if (++s == S) { s = 0; ph ^= 1u; }
-        if (++ku == KT) ku = 0;
+        if (++ku == KT) {
+          ku = 0;
+          if (++mt == MT) mt = 0;
+        }
       }
       const int first = issued > S ? issued - S : 0;
       for (int i = first; i < issued; ++i)
@@ -397,16 +408,18 @@ __global__ void __launch_bounds__(kSmThreads, 1)
 
         // ---- epilogue (even-half warps): fp16 Y, or fp32 partial + reduction ----
         // accumulator d of block nb: column col_r + 8*(d >> 1), token 8nb + tok[d & 1]
-        const size_t y_col0 = (size_t)tile * kTileN + col_r;
+        const size_t y_col0 = (size_t)(tile / p.m_tiles) * kTileN + col_r;
+        const int m_base = (tile - (tile / p.m_tiles) * p.m_tiles) * p.bn;   // first token of the m-tile
         if (whole) {
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
             for (int d = 0; d < 4; ++d) {
               const int m = 8 * nb + ((d & 1) ? tok1 : tok0);
-              if (m < p.M && W4A16_IN_RANGE(p.status, (size_t)m * p.N + y_col0 + 8 * (d >> 1), 1,
-                                            (size_t)p.M * p.N, 11))
-                p.Y[(size_t)m * p.N + y_col0 + 8 * (d >> 1)] =
+              if (m_base + m < p.M &&
+                  W4A16_IN_RANGE(p.status, (size_t)(m_base + m) * p.N + y_col0 + 8 * (d >> 1), 1,
+                                 (size_t)p.M * p.N, 11))
+                p.Y[(size_t)(m_base + m) * p.N + y_col0 + 8 * (d >> 1)] =
                     __half_as_ushort(__float2half_rn(acc[nb][d]));
             }
         } else {
@@ -479,9 +492,10 @@ __global__ void __launch_bounds__(kSmThreads, 1)
 #pragma unroll
               for (int d = 0; d < 4; ++d) {
                 const int m = 8 * nb + ((d & 1) ? tok1 : tok0);
-                if (m < p.M && W4A16_IN_RANGE(p.status, (size_t)m * p.N + y_col0 + 8 * (d >> 1), 1,
-                                              (size_t)p.M * p.N, 11))
-                  p.Y[(size_t)m * p.N + y_col0 + 8 * (d >> 1)] =
+                if (m_base + m < p.M &&
+                    W4A16_IN_RANGE(p.status, (size_t)(m_base + m) * p.N + y_col0 + 8 * (d >> 1), 1,
+                                   (size_t)p.M * p.N, 11))
+                  p.Y[(size_t)(m_base + m) * p.N + y_col0 + 8 * (d >> 1)] =
                       __half_as_ushort(__float2half_rn(acc[nb][d]));
               }
           }

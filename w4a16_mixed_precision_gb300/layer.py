@@ -10,8 +10,12 @@ bias and no other arithmetic outside the kernel.
 
 With sparse=True the weights must be 2:4 ("Marlin", section "支持 2:4 稀疏加速":
 two of every four weights zero at fixed positions): the layer also holds the
-2:4 form and serves batches of up to 32 rows with marlin_sparse_gemm, larger
-ones with the dense kernel.
+2:4 form.  marlin_sparse_gemm serves every M, but above 32 rows each further
+32-row m-tile dequantises the weights again, and on GB300 the dense tcgen05
+kernel was measured faster there (0.52-0.99x for the 2:4 path at M = 33..256
+on the Llama-2-7B shapes, against 0.98-1.15x in its favour at M = 32).  So the
+layer sends batches of up to 32 rows to marlin_sparse_gemm and larger ones to
+the dense kernel.
 """
 from __future__ import annotations
 
