@@ -62,6 +62,8 @@ static_assert(kThreads == 32 * (kFirstDqWarp + kNumDqWarps), "block size");
 // the producer and the MMA issuer are single threads, so any integer division
 // on their path sits directly on the critical path of the whole CTA.
 
+// ZP: explicit zero points (else the implicit zero 8 folds into constants).
+template <bool ZP>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_gemm_kernel(const __grid_constant__ CUtensorMap x_map, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -298,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;             // TMEM lane quarter this warp may touch
     const int row = quarter * 32 + lane;      // epilogue: output column within the tile
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const bool has_zeros = p.zeros != nullptr;
+
     // dequantisation: this thread holds fragment lane `lane` of the two 16-column
     // groups 2*quarter and 2*quarter+1, i.e. columns c0 + {0, 8, 16, 24}
     const int c0 = 32 * quarter + (lane >> 2);
@@ -308,25 +310,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t z_shift = (uint32_t)(c0 & 1) * 4;
     const int a_slots = p.a_slots;
     const uint32_t a_cols = (uint32_t)cpu * (kChunkK / 2);
-    int s = 0, a = 0, seg = 0;
+    // (s, a) are the stage and A slot of unit r (the unit's index in the
+    // stripe), with their phases; advance(n) moves them n units on.  When the
+    // stage count is a multiple of 4 each warpgroup visits only its own units
+    // r = wg, wg + 4, ...: its stages and its A slots are then used by no
+    // other warpgroup between two of its visits (the slot's next user after
+    // unit r is unit r + a_slots, again after this warpgroup's own release),
+    // so one phase of look-ahead is enough.  Otherwise (full_all) every warp
+    // waits on and releases every stage, own or not.
+    int s = 0, a = 0, seg = 0, r = 0;
     uint32_t ph = 0, aph = 0;
+    auto advance = [&](int n) {
+      s += n;
+      while (s >= S) { s -= S; ph ^= 1u; }
+      a += n;
+      while (a >= a_slots) { a -= a_slots; aph ^= 1u; }
+      r += n;
+    };
+    const int stride = p.full_all ? 1 : kNumDqWG;
+    if (!p.full_all) advance(wg);
     int u = u_begin, ku = ku_begin, tile = tile_begin;
     bool ok = true;
     while (ok && u < u_end) {
       const int seg_len = min(u_end - u, KT - ku);
+      const int r_end = u - u_begin + seg_len;  // first unit of the next segment
       const int mt = tile / p.n_tiles;
       const int nt = tile - mt * p.n_tiles;
       // ---- mainloop: dequantise this warpgroup's units into TMEM ----
-      for (int i = 0; i < seg_len; ++i) {
-        const bool mine = ((u - u_begin + i) & (kNumDqWG - 1)) == wg;
-        if (!mine && p.full_all) {
-          // track every stage: wait for it and release it, so that the ring can
-          // neither run a phase ahead of this warp nor lap it
+      for (; r < r_end; advance(stride)) {
+        const bool mine = (r & (kNumDqWG - 1)) == wg;
+        if (!mine) {
+          // full_all: track every stage: wait for it and release it, so that
+          // the ring can neither run a phase ahead of this warp nor lap it
           if (!wait_warp(bar(ctrl->full[s]), ph, wc)) { ok = false; break; }
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(ctrl->empty[s]));
-        }
-        if (mine) {
+        } else {
           if (!wait_warp(bar(ctrl->full[s]), ph, wc)) { ok = false; break; }
           const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
           // a unit (cpu <= 2 chunks of 64 rows, group >= 128) lies in one group row
@@ -335,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint4 w0 = cok ? lds128(st + code_off) : z4;        // chunk 0, group 2q
           const uint4 w1 = cok ? lds128(st + code_off + 512) : z4;  // chunk 0, group 2q+1
           uint32_t z0 = 8, z1 = 8, z2 = 8, z3 = 8;
-          if (has_zeros && W4A16_SMEM_OK(p, raw_addr, st + zr_off, 13, 26)) {
+          if (ZP && W4A16_SMEM_OK(p, raw_addr, st + zr_off, 13, 26)) {
             z0 = (lds_u8(st + zr_off) >> z_shift) & 0xFu;
             z1 = (lds_u8(st + zr_off + 4) >> z_shift) & 0xFu;
             z2 = (lds_u8(st + zr_off + 8) >> z_shift) & 0xFu;
@@ -377,8 +396,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(ctrl->afull[a]));
         }
-        if (++a == a_slots) { a = 0; aph ^= 1u; }
-        if (++s == S) { s = 0; ph ^= 1u; }
       }
       if (!ok) break;
 
@@ -500,7 +517,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t gemm_set_smem_limit(int bytes) {
-  return cudaFuncSetAttribute(w4a16_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  cudaError_t e = cudaFuncSetAttribute(w4a16_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(w4a16_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  return e;
 }
 
 cudaError_t launch_gemm(const CUtensorMap& x_map, const GemmParams& p, int grid, uint32_t smem_bytes,
@@ -515,7 +536,8 @@ cudaError_t launch_gemm(const CUtensorMap& x_map, const GemmParams& p, int grid,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, w4a16_gemm_kernel, x_map, p);
+  if (p.zeros) return cudaLaunchKernelEx(&cfg, w4a16_gemm_kernel<true>, x_map, p);
+  return cudaLaunchKernelEx(&cfg, w4a16_gemm_kernel<false>, x_map, p);
 }
 
 }  // namespace w4a16
