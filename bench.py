@@ -653,10 +653,13 @@ def end_to_end(problems, packed, ws, plans, dev, args, step_bytes, call):
     """The step through the public API with host buffers: every step copies all
     of its activations in from pinned host memory (one copy of one buffer that
     holds every problem's X), makes the 24 marlin_gemm calls (gemm_into), and
-    copies every Y back (one copy), on one stream."""
+    copies every Y back (one copy), on one stream, then synchronises.
+
+    Reported value: the step captured once as a CUDA graph (the two copies and
+    the 24 library calls, as a decode loop replays its step) and replayed per
+    step.  `eager`: the same step issued call by call from Python."""
     import torch
 
-    import w4a16_mixed_precision_gb300 as w4
     xs_n = [p.M * p.K for p in problems]
     ys_n = [p.M * p.N for p in problems]
 
@@ -679,26 +682,47 @@ def end_to_end(problems, packed, ws, plans, dev, args, step_bytes, call):
     dy = [dyb[o:o + n].view(p.M, p.N) for p, o, n in zip(problems, yo, ys_n)]
     steps = max(3, min(args.steps, 200))
 
-    def one(plan):
+    def issue(plan):
         dxb.copy_(hx, non_blocking=True)
         for i, c in plan:
             p = problems[i]
             lk = (p.K, p.N, p.group, p.asym)
             call(dx[i], packed[lk][c], ws[lk], dy[i])
         hy.copy_(dyb, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
 
-    for k in range(3):
-        one(plans[k % len(plans)])
-    t0 = time.perf_counter()
-    for k in range(steps):
-        one(plans[k % len(plans)])
-    dt = (time.perf_counter() - t0) / steps
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        # eager: call by call
+        for k in range(3):
+            issue(plans[k % len(plans)])
+            stream.synchronize()
+        t0 = time.perf_counter()
+        for k in range(steps):
+            issue(plans[k % len(plans)])
+            stream.synchronize()
+        dt_eager = (time.perf_counter() - t0) / steps
+        # graph: one capture per rotation phase, replayed per step
+        graphs = []
+        for plan in plans:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                issue(plan)
+            graphs.append(g)
+        for k in range(3):
+            graphs[k % len(graphs)].replay()
+            stream.synchronize()
+        t0 = time.perf_counter()
+        for k in range(steps):
+            graphs[k % len(graphs)].replay()
+            stream.synchronize()
+        dt = (time.perf_counter() - t0) / steps
     return {"value": step_bytes / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": xt * 2,
             "d2h_bytes_per_step": yt * 2, "ms_per_step": dt * 1e3, "steps": steps,
-            "path": f"per step: one H2D copy of all activations from pinned host memory, the {len(problems)} "
-                    f"library calls ({call.__name__}) through the Python binding, one D2H copy of all outputs; "
-                    "host wall clock around the whole step, synchronised"}
+            "path": f"per step: one CUDA-graph replay holding the H2D copy of all activations from pinned host "
+                    f"memory, the {len(problems)} library calls ({call.__name__}) and the D2H copy of all "
+                    "outputs, then a stream synchronisation; host wall clock around each whole step",
+            "eager": {"value": step_bytes / dt_eager / 1e9, "ms_per_step": dt_eager * 1e3,
+                      "path": "the same step issued call by call through the Python binding"}}
 
 
 def main():

@@ -116,9 +116,11 @@ __device__ __forceinline__ long long stripe_owner(long long u, long long U, long
 // CTA publishes at most one partial tile (from its first segment, then goes on
 // without waiting) and reduces at most one (at its very end), and no CTA ever
 // waits for a CTA that is itself waiting: the wait graph has no cycles.
-// Contributors publish their partial words tagged (st_partial) and add one to
-// the tile's arrival counter; the reducer polls the words it needs and the
-// counter, both with bounded waits, and leaves words and counter zeroed.
+// Contributors publish their partial words tagged (st_partial); the reducer
+// polls the words it needs with bounded waits and leaves them zeroed.  The
+// tcgen05 kernel's contributors also add one to the tile's arrival counter,
+// which its reducer waits for (and re-zeroes); the warp-level kernel's reducer
+// relies on the tags alone.
 
 __device__ __forceinline__ long long tile_reducer(long long tile, long long KT, long long U,
                                                   long long G) {
