@@ -163,12 +163,17 @@ GemmPlan make_plan(int M, int K, int N, int group, int sms, int smem_optin, bool
   g.upg = (group > g.cpu * kChunkK) ? group / (g.cpu * kChunkK) : 1;
   g.units = (long long)g.m_tiles * g.n_tiles * g.kt;
   g.grid = (int)(g.units < sms ? g.units : sms);
-  // Warp-level kernel with short stripes (under 15 units per SM): one SM in 19
-  // is left idle.  Measured with back-to-back calls on 152 SMs, 144 CTAs beat
-  // 152 by 2-10% on 4096x4096, 4096x12288, 11008x4096, 2048x5632 and
-  // 13824x5120 (M = 1 and 16) and tied on 8192x8192; from about 15 units per
-  // SM (4096x22016, 5120x15360) the full grid is faster.
-  if (warp_level && g.grid == sms && g.units < 15LL * sms) g.grid = sms - sms / 19;
+  // Short stripes (under 240 KB of weight codes per SM): one SM in 19 is left
+  // idle.  Measured with back-to-back calls on 152 SMs, 144 CTAs beat 152 by
+  // 2-10% on 4096x4096, 4096x12288, 11008x4096, 2048x5632, 13824x5120 and
+  // 8192x8192 (warp-level kernel at M = 1 and 16, tcgen05 kernel at M = 32..64)
+  // and tied at 215-250 KB per SM; above that (4096x22016, 8192x10240) the
+  // full grid is faster.
+  {
+    const long long unit_code_bytes =
+        (long long)g.cpu * (sparse ? kSpChunkCodeBytes + kSpChunkMetaBytes : kChunkCodeBytes);
+    if (g.grid == sms && g.units * unit_code_bytes < 240LL * 1024 * sms) g.grid = sms - sms / 19;
+  }
   const size_t x_chunk = (size_t)g.bn * 128;
   const size_t chunk_w = sparse ? (size_t)(kSpChunkCodeBytes + kSpChunkMetaBytes) : kChunkCodeBytes;
   const size_t stage = g.cpu * (x_chunk + chunk_w) +
