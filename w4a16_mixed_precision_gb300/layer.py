@@ -29,7 +29,7 @@ from .formats import awq_to_gptq
 class W4A16Linear(torch.nn.Module):
     """y[..., N] = x[..., K] . dequant(W)[K, N], fp16 in and out, fp32 accumulation."""
 
-    SPARSE_MAX_M = 32  # largest batch of the 2:4 path (the warp-level kernel's range)
+    SPARSE_MAX_M = 32  # largest batch sent to the 2:4 path (above it the dense kernel measured faster)
 
     def __init__(self, qweight: torch.Tensor, scales: torch.Tensor, qzeros: torch.Tensor | None = None,
                  group: int = 128, device=None, sparse: bool = False):
