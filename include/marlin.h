@@ -112,8 +112,9 @@ marlin_status_t marlin_repack(const int32_t* q, const uint16_t* scales, const in
  * "Key Techniques", item "Striped Partitioning", names the global reduction
  * this scratch serves; the size query itself has no page passage.
  * The workspace holds one fp32 partial tile per CTA for the striped
- * partition's global reduction, one arrival counter per output tile and a
- * status word.  A buffer sized for M also serves every smaller M with the
+ * partition's global reduction, one int per output tile (read only by
+ * bounds-checked MARLIN_DEBUG builds, whose reducers wait for it to be
+ * non-negative; it must start at zero) and a status word.  A buffer sized for M also serves every smaller M with the
  * same K, N, group, with either kernel (marlin_gemm_ex).  Host-only; queries
  * the device attributes once.  bytes: host pointer, written.
  */

@@ -3,14 +3,10 @@
 Every wait inside the kernels gives up after 2 s of global time, records
 MARLIN_ERR_TIMEOUT in the workspace's status word, and lets the kernel drain
 its own copies and MMAs and exit.  The waits are made to expire through a word
-that nothing sets:
-
-* tcgen05 kernel: its reducers wait for the tile's arrival counter to reach
-  the number of contributors; the counters are preset to a value the
-  contributors can never raise that far.
-* warp-level kernel (dense and 2:4): its reducers rely on the tagged partial
-  words alone, but in the bounds-checked (MARLIN_DEBUG) build they also wait
-  for the tile's counter word to be non-negative; it is preset negative.
+that nothing sets: the reducers of both kernels rely on the tagged partial
+words alone, but in the bounds-checked (MARLIN_DEBUG) build they also wait for
+their tile's word in the workspace's counter block to be non-negative; the
+tests preset it negative and call through that build's C ABI.
 
 The host must then read MARLIN_ERR_TIMEOUT, and the context must stay usable:
 after re-zeroing the workspace the same call gives the oracle's result.
@@ -52,38 +48,16 @@ def _hold(ws_buf, n_tiles):
     ws_buf[256:256 + 4 * n_tiles].view(torch.int32).fill_(-1000000)
 
 
-def test_expired_wait_tcgen05_kernel():
-    import w4a16_mixed_precision_gb300 as w4
-    from w4a16_mixed_precision_gb300 import _binding as b
-    p = Problem("timeout", 64, 4096, 1024, 128, False)
-    inp = make_inputs(p)
-    dev = torch.device("cuda", 0)
-    pw = w4.repack(torch.from_numpy(inp.Qp).to(dev), torch.from_numpy(inp.S).to(dev), None, 128)
-    x = torch.from_numpy(inp.X).to(dev)
-    ws = w4.Workspace(p.M, p.K, p.N, p.group)
-    _hold(ws.buf, p.N // 128)
-    w4.gemm(x, pw, ws)
-    torch.cuda.synchronize()
-    rc = b.last_device_status(ws.ptr, _stream())
-    assert rc == b.ERR_TIMEOUT, b.status_string(rc)
-    # the status word was cleared by the read; the context still works
-    ws.buf.zero_()
-    y = w4.gemm(x, pw, ws)
-    torch.cuda.synchronize()
-    assert w4.device_status(ws) == 0
-    ok, err, ratio = oracle.within_tolerance(y.cpu().numpy(), oracle.w4a16(inp.X, inp.Qp, inp.S, None, 128, p.N))
-    assert ok, f"max abs err {err}"
-
-
 def _workspace(lib, M, K, N, g):
     nb = ctypes.c_size_t()
     assert lib.marlin_workspace_bytes(M, K, N, g, 0, ctypes.byref(nb)) == 0
     return torch.zeros(nb.value, dtype=torch.uint8, device="cuda")
 
 
-def test_expired_wait_warp_kernel(dbg):
+@pytest.mark.parametrize("M,kernel", [(1, 1), (64, 2)])   # warp-level kernel, tcgen05 kernel
+def test_expired_wait_dense(dbg, M, kernel):
     import w4a16_mixed_precision_gb300 as w4
-    M, K, N, g = 1, 4096, 1024, 128
+    K, N, g = 4096, 1024, 128
     inp = make_inputs(Problem("timeout", M, K, N, g, False))
     dev = torch.device("cuda", 0)
     pw = w4.repack(torch.from_numpy(inp.Qp).to(dev), torch.from_numpy(inp.S).to(dev), None, g)
@@ -94,7 +68,7 @@ def test_expired_wait_warp_kernel(dbg):
     def call():
         base = pw.buf.data_ptr()
         return dbg.marlin_gemm_ex(x.data_ptr(), base, base + pw.off_scales, None, y.data_ptr(), M, K, N, g,
-                                  ws.data_ptr(), ws.numel(), 1, _stream())
+                                  ws.data_ptr(), ws.numel(), kernel, _stream())
 
     _hold(ws, N // 128)
     assert call() == 0

@@ -117,10 +117,11 @@ __device__ __forceinline__ long long stripe_owner(long long u, long long U, long
 // without waiting) and reduces at most one (at its very end), and no CTA ever
 // waits for a CTA that is itself waiting: the wait graph has no cycles.
 // Contributors publish their partial words tagged (st_partial); the reducer
-// polls the words it needs with bounded waits and leaves them zeroed.  The
-// tcgen05 kernel's contributors also add one to the tile's arrival counter,
-// which its reducer waits for (and re-zeroes); the warp-level kernel's reducer
-// relies on the tags alone.
+// polls the words it needs with bounded waits and leaves them zeroed.  No
+// arrival count is kept: the tags alone tell the reducer a word is final.  The
+// workspace's counter block (one int per tile) is read only by bounds-checked
+// (MARLIN_DEBUG) builds, whose reducers wait for their tile's word to be
+// non-negative, so that a test can make that wait expire.
 
 __device__ __forceinline__ long long tile_reducer(long long tile, long long KT, long long U,
                                                   long long G) {

@@ -44,7 +44,7 @@ struct Ctrl {
   uint64_t dfull;
   uint64_t dempty;
   uint64_t drain[2];
-  uint64_t red_go;      // leader -> dequant warps: all partials published (reducer)
+  uint64_t red_go;      // leader -> dequant warps: the reducer may write Y
   uint32_t tmem_base;
   int abort;
 };
@@ -409,14 +409,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long c_last = stripe_owner((long long)tile * KT + KT - 1, U, G);
       const bool reducer = !whole && (long long)blockIdx.x == c_first;
       if (reducer && dq == 0) {
-        // reducer (this is its last segment): the leader waits for the count
-        // of contributors, while every thread polls its own words of their
-        // partial tiles (a tagged word is final once non-zero)
+        // reducer (this is its last segment): every thread polls its own words
+        // of the contributors' partial tiles (a tagged word is final once
+        // non-zero, so no arrival count is needed; measured 0.3-0.7 us less per
+        // call at M = 32..128).  In a MARLIN_DEBUG build the leader first waits
+        // (bounded) for the tile's word in the counter block to be
+        // non-negative: nothing writes it, so a test can hold the reduction by
+        // presetting it negative and make the wait expire.
         if (lane == 0) {
+#ifdef MARLIN_DEBUG
           if (W4A16_IN_RANGE(p.status, (const char*)&p.counters[tile] - (const char*)p.status, 4, p.ws_bytes,
-                             32) &&
-              wait_counter(&p.counters[tile], (int)(c_last - c_first), wc))
-            p.counters[tile] = 0;  // leave the workspace zeroed for the next call
+                             32))
+            wait_counter(&p.counters[tile], 0, wc);
+#endif
           mbar_arrive(bar(ctrl->red_go));
         }
         __syncwarp();
@@ -492,11 +497,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(ctrl->dempty));
-      // contributor (this is its first segment): its tagged words are its
-      // publication; count it in and go on without waiting
-      if (!whole && !reducer && dq == 0 && lane == 0 &&
-          W4A16_IN_RANGE(p.status, (const char*)&p.counters[tile] - (const char*)p.status, 4, p.ws_bytes, 32))
-        red_relaxed_gpu_add(&p.counters[tile], 1);
       ++seg;
       u += seg_len;
       ku = 0;
