@@ -76,13 +76,13 @@ def kernel_source_digest() -> str:
 
 
 def kernel_names(problems) -> str:
-    """The fused kernels a workload launches: the warp-level path for M <= 24,
+    """The fused kernels a workload launches: the warp-level path for M <= 16,
     the tcgen05 path above (the library's default split); 2:4 weights: the
     sparse instantiation of the warp-level kernel at every M <= 32."""
     if any(p.sparse for p in problems):
         return "w4a16_small_m_kernel (2:4-sparse instantiation, mma.sp)"
-    small = any(p.M <= 24 for p in problems)
-    big = any(p.M > 24 for p in problems)
+    small = any(p.M <= 16 for p in problems)
+    big = any(p.M > 16 for p in problems)
     return " + ".join(n for n, on in (("w4a16_small_m_kernel", small), ("w4a16_gemm_kernel", big)) if on)
 
 

@@ -160,7 +160,7 @@ marlin_status_t marlin_gemm(const uint16_t* X, const void* packed, const uint16_
  * design; this library has two for the same operation: a warp-level one
  * (mma.sync fed from registers, M <= 32) and a tcgen05 one (operand in tensor
  * memory, any M).  MARLIN_KERNEL_AUTO picks by M (the warp-level kernel for
- * M <= 24, or the bound set by the environment variable W4A16_SMALL_M_MAX,
+ * M <= 16, or the bound set by the environment variable W4A16_SMALL_M_MAX,
  * 0..32).
  */
 typedef enum {

@@ -1,6 +1,6 @@
 """Both fused kernels at batch sizes outside their default range.
 
-The library sends M <= 24 to the warp-level kernel and larger M to the tcgen05
+The library sends M <= 16 to the warp-level kernel and larger M to the tcgen05
 kernel; W4A16_SMALL_M_MAX (read once per process) moves that split.  Each case
 runs in a child process with the split moved, so that the tcgen05 kernel is
 checked at decode batches down to M = 1 and the warp-level kernel up to its

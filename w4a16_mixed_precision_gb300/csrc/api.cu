@@ -72,16 +72,16 @@ marlin_status_t check_shape_group(int K, int N, int* group) {
   return *group % 128 == 0 ? MARLIN_OK : MARLIN_ERR_UNSUPPORTED;
 }
 
-// Largest M served by the small-batch kernel (mma.sync path); larger M uses the
-// tcgen05 kernel.  W4A16_SMALL_M_MAX overrides it (0 disables the small path).
-// Largest M served by the warp-level kernel (measured crossover: at M = 32 the
-// tcgen05 kernel is faster on every decode shape, at M <= 24 the warp-level
-// one).  W4A16_SMALL_M_MAX overrides it (0..32), e.g. to test either kernel at
-// any M.
+// Largest M served by the warp-level kernel (mma.sync fed from registers);
+// larger M uses the tcgen05 kernel.  Measured crossover (ncu, each kernel
+// forced, on 4096x12288 and 8192x8192): the warp-level kernel is 1.07-1.26x
+// faster at M <= 16, the two tie at M = 24 (tcgen05 1.01-1.02x) and the tcgen05
+// kernel is 1.12x faster at M = 32.  W4A16_SMALL_M_MAX overrides it (0..32,
+// 0 disables the warp-level path), e.g. to test either kernel at any M.
 int small_m_max() {
   static int v = [] {
     const char* e = getenv("W4A16_SMALL_M_MAX");
-    int x = e ? atoi(e) : 24;
+    int x = e ? atoi(e) : 16;
     return x < 0 ? 0 : (x > kMaxWarpM ? kMaxWarpM : x);
   }();
   return v;

@@ -1,5 +1,5 @@
 // small_m.cu -- the fused W4A16 matrix multiply for small batches (M <= 32; by
-// default the library sends M <= 24 here and larger batches to gemm.cu; the
+// default the library sends M <= 16 here and larger batches to gemm.cu; the
 // 2:4-sparse instantiation serves every M, in m-tiles of 32 tokens):
 // Y[M][N] = X[M][K] . dequant(W)[K][N] on the warp-level tensor-core path.
 //

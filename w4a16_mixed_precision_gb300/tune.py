@@ -1,6 +1,6 @@
 """Per-shape kernel choice by measurement.
 
-marlin_gemm picks its kernel by M alone (the warp-level one up to M = 24).
+marlin_gemm picks its kernel by M alone (the warp-level one up to M = 16).
 This tuner times both kernels on the caller's own weights and workspace for a
 given (M, K, N, group, zeros) and remembers the faster one, for callers whose
 shapes sit near the crossover.  Timing: CUDA graphs of `reps` back-to-back
