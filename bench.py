@@ -748,7 +748,11 @@ def end_to_end(problems, packed, ws, plans, dev, args, step_bytes, call):
             graphs[k % len(graphs)].replay()
             stream.synchronize()
         dt = (time.perf_counter() - t0) / steps
-    return {"value": step_bytes / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": xt * 2,
+        # the host copies of the last step's outputs must be the device's outputs
+        dyh, dxh = dyb.cpu(), dxb.cpu()
+        checked = all(torch.equal(hy[o:o + n], dyh[o:o + n]) for o, n in zip(yo, ys_n)) and \
+            all(torch.equal(hx[o:o + n], dxh[o:o + n]) for o, n in zip(xo, xs_n))
+    return {"value": step_bytes / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": xt * 2, "copies_checked": checked,
             "d2h_bytes_per_step": yt * 2, "ms_per_step": dt * 1e3, "steps": steps,
             "path": f"per step: one CUDA-graph replay holding the H2D copies of all activations from pinned "
                     f"host memory (the first call's X on the compute stream, the rest in one copy on a side "
