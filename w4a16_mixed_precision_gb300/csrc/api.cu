@@ -410,7 +410,7 @@ marlin_status_t marlin_workspace_bytes(int M, int K, int N, int group, int devic
                                MARLIN_KERNEL_WARP);
   if (w.ws_bytes > need) need = w.ws_bytes;
   if (m > kMaxWarpM) {
-    // the 2:4 path at this M: m-tiles of 32 tokens, one counter per (tile, m-tile)
+    // the 2:4 path at this M: m-tiles of 32 tokens, one int per (tile, m-tile)
     const GemmPlan sp = make_plan(m, K, N, group, d->sms, d->smem_optin, true, MARLIN_KERNEL_WARP, true);
     if (sp.ws_bytes > need) need = sp.ws_bytes;
   }

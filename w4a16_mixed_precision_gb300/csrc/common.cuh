@@ -134,10 +134,6 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
   return v;
 }
 
-__device__ __forceinline__ void red_relaxed_gpu_add(int* p, int v) {
-  asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 // Partial tiles of split tiles are published element by element: a partial
 // value v is stored as bits(v) ^ kPartTag, so that a zero word means "not
 // written yet" (the workspace starts zeroed and the reducer re-zeroes what it

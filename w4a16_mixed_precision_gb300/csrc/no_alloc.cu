@@ -1,7 +1,7 @@
 // no_alloc.cu -- marlin_gemm_no_alloc: the fused W4A16 multiply for callers
 // that cannot allocate device memory.  The scratch that marlin_gemm keeps in
-// the caller's workspace (status word, tile arrival counters, fp32 partial
-// tiles of the split reduction) lives here in a library-owned static device
+// the caller's workspace (status word, one int per tile, fp32 partial tiles of
+// the split reduction) lives here in a library-owned static device
 // array instead; every GPU that loads the library holds it until the process
 // exits.
 #include <cuda_runtime.h>
@@ -61,8 +61,9 @@ extern "C" marlin_status_t marlin_gemm_no_alloc(const uint16_t* X, const void* p
   void* scratch = nullptr;
   if ((s = scratch_on(dev, &scratch)) != MARLIN_OK) return s;
   // The array keeps the previous call's contents.  Everything this call uses
-  // must start at zero: the status word, the tile arrival counters, and the
-  // partial-tile words (a zero word means "not yet written").  A completed call
+  // must start at zero: the status word, the per-tile ints (which a
+  // bounds-checked build's reducers wait on), and the partial-tile words (a
+  // zero word means "not yet written").  A completed call
   // leaves them zeroed, but one whose kernel gave up on a bounded wait may not,
   // and this entry point does not report that; so clear this call's region.
   if (cudaMemsetAsync(scratch, 0, need, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
