@@ -32,10 +32,10 @@ SMALL_CASES = [
     (1, 128, 128, 128, False),
     (1, 4096, 384, 128, False),
     (5, 256, 384, 128, True),
-    (16, 1024, 512, 128, False),
-    (17, 512, 256, 128, True),
-    (24, 1024, 640, 128, False),       # largest batch of the warp-level kernel by default
-    (25, 1024, 640, 128, True),        # smallest batch of the tcgen05 kernel by default
+    (16, 1024, 512, 128, False),       # largest batch of the warp-level kernel by default
+    (17, 512, 256, 128, True),         # smallest batch of the tcgen05 kernel by default
+    (24, 1024, 640, 128, False),
+    (25, 1024, 640, 128, True),
     (32, 2048, 1024, 128, False),
     (33, 1024, 640, 1024, True),       # one scale per column, ragged M
     (48, 2048, 768, 128, True),
@@ -44,6 +44,8 @@ SMALL_CASES = [
     (80, 2048, 384, 256, False),       # group 256, tcgen05 kernel
     (300, 1024, 256, 1024, True),      # one scale per column, two m-tiles
     (100, 768, 256, 128, False),
+    (12, 384, 256, 128, True),         # K % 256 = 128: 128-row units, two token blocks
+    (16, 640, 384, 128, False),
     (128, 1024, 384, 128, True),
     (200, 512, 1280, 128, False),
     (256, 512, 384, 128, False),

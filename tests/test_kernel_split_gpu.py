@@ -60,7 +60,8 @@ def test_tcgen05_kernel_at_decode_batches():
 
 
 def test_warp_level_kernel_up_to_its_largest_batch():
-    cases = [(25, 1024, 640, 128, True), (32, 2048, 1024, 128, False), (31, 4096, 384, 4096, True)]
+    cases = [(25, 1024, 640, 128, True), (32, 2048, 1024, 128, False), (31, 4096, 384, 4096, True),
+             (28, 384, 256, 128, True)]   # the last: 128-row units (K % 256 = 128), four token blocks
     for M, ok, err in _run(32, cases):
         assert ok, f"M={M}: max abs err {err}"
 
