@@ -225,10 +225,9 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         const uint32_t st = stage0 + (uint32_t)s * p.stage_bytes;
         const uint32_t fb = bar(ctrl->full[s]);
         mbar_arrive_expect_tx(fb, tx);
-        const int k0 = ku * cpu * kChunkK;
-        for (int j = 0; j < cpu; ++j)
-          if (W4A16_SMEM_OK(p, raw_addr, st + (uint32_t)j * p.x_chunk_bytes, p.x_chunk_bytes, 6))
-            tma_load_2d(st + (uint32_t)j * p.x_chunk_bytes, &x_map, k0 + j * kChunkK, mt * p.bn, fb, pol);
+        // one 3-D box: the unit's cpu chunks of 64 columns, bn token rows each
+        if (W4A16_SMEM_OK(p, raw_addr, st, (uint32_t)cpu * p.x_chunk_bytes, 6))
+          tma_load_3d(st, &x_map, 0, mt * p.bn, ku * cpu, fb, pol);
         ++issued;
         if (++s == S) { s = 0; ph ^= 1u; }
         if (++ku == KT) {
