@@ -176,16 +176,23 @@ GemmPlan make_plan(int M, int K, int N, int group, int sms, int smem_optin, bool
   // least 4/5 of the SMs that gives every CTA the same whole number of units
   // and splits every column tile evenly, if there is one.  Measured on
   // 4096x4096: 128 CTAs against 144, warp-level kernel M = 1 6.22 -> 5.85 us,
-  // M = 16 7.98 -> 7.64 us, tcgen05 kernel M = 32 11.09 -> 9.71 us; at 256 KB
-  // per CTA (8192x8192) the even split was 4% slower than 144 CTAs.
+  // M = 16 7.98 -> 7.64 us, tcgen05 kernel M = 32 11.09 -> 9.71 us.  The
+  // 128 KB bound holds for the warp-level kernel only: at 256 KB per CTA
+  // (8192x8192) its even split was 2-4% slower than 144 CTAs, while the
+  // tcgen05 kernel's was faster (8192x8192 at M = 32 / 64 / 128: 17.22 /
+  // 20.10 / 28.31 -> 16.41 / 18.44 / 25.52 us), its epilogue per piece of a
+  // split tile (accumulator read-back and partial write of bn x 128 fp32)
+  // costing far more than the warp-level kernel's.
   {
     const long long unit_code_bytes =
         (long long)g.cpu * (sparse ? kSpChunkCodeBytes + kSpChunkMetaBytes : kChunkCodeBytes);
+    const bool capped = g.kind == kKernelSmallM;
     if (g.grid == sms && g.units * unit_code_bytes < 240LL * 1024 * sms) {
       g.grid = sms - sms / 19;
       for (int G = sms; G * 5 >= sms * 4; --G) {
         const long long per = g.units / G;
-        if (g.units % G == 0 && g.kt % per == 0 && per * unit_code_bytes <= 128LL * 1024) {
+        if (g.units % G == 0 && g.kt % per == 0 &&
+            (!capped || per * unit_code_bytes <= 128LL * 1024)) {
           g.grid = G;
           break;
         }
