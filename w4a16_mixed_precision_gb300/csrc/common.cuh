@@ -159,26 +159,45 @@ __device__ __forceinline__ uint32_t ld_partial_raw(const float* p) {
 
 __device__ __forceinline__ float partial_value(uint32_t raw) { return __uint_as_float(raw ^ kPartTag); }
 
+// Loads of the words base[q * stride + off[i]] (q < nq, i < NO) into
+// raw[q * NO + i] (0 for q >= nq), issued together; a reducer issues them
+// ahead of other work so that their round trip overlaps it.
+template <int NQ, int NO>
+__device__ __forceinline__ void issue_partials(const float* base, size_t stride, const uint32_t (&off)[NO],
+                                               int nq, uint32_t (&raw)[NQ * NO]) {
+#pragma unroll
+  for (int q = 0; q < NQ; ++q)
+#pragma unroll
+    for (int i = 0; i < NO; ++i) raw[q * NO + i] = q < nq ? ld_partial_raw(base + q * stride + off[i]) : 0u;
+}
+
 // Bounded poll until the words base[q * stride + off[i]] (q < nq, i < NO) are
 // all written, into raw[q * NO + i]; returns false on timeout (recorded) or
-// when the CTA is aborting.
+// when the CTA is aborting.  With preloaded, raw already holds the words'
+// values from issue_partials (a zero word is not written yet, and is loaded
+// again); otherwise every word is loaded here.
 template <int NQ, int NO>
 __device__ __forceinline__ bool poll_partials(const float* base, size_t stride, const uint32_t (&off)[NO],
-                                              int nq, uint32_t (&raw)[NQ * NO], const WaitCtx& c) {
+                                              int nq, uint32_t (&raw)[NQ * NO], const WaitCtx& c,
+                                              bool preloaded = false) {
+  if (!preloaded) {
 #pragma unroll
-  for (int i = 0; i < NQ * NO; ++i) raw[i] = 0u;
+    for (int i = 0; i < NQ * NO; ++i) raw[i] = 0u;
+  }
   uint64_t t0 = 0;
 #pragma unroll 1
   for (int attempt = 0;; ++attempt) {
     // issue every missing word's load first, then test them all: the loads
     // are in flight together (one round trip per attempt)
+    if (attempt > 0 || !preloaded) {
 #pragma unroll
-    for (int q = 0; q < NQ; ++q)
-      if (q < nq) {
+      for (int q = 0; q < NQ; ++q)
+        if (q < nq) {
 #pragma unroll
-        for (int i = 0; i < NO; ++i)
-          if (raw[q * NO + i] == 0u) raw[q * NO + i] = ld_partial_raw(base + q * stride + off[i]);
-      }
+          for (int i = 0; i < NO; ++i)
+            if (raw[q * NO + i] == 0u) raw[q * NO + i] = ld_partial_raw(base + q * stride + off[i]);
+        }
+    }
     bool done = true;
 #pragma unroll
     for (int q = 0; q < NQ; ++q)

@@ -406,14 +406,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
 
       // ---- epilogue: accumulators -> fp16 Y, or fp32 partial tile ----
-      if (!wait_warp(bar(ctrl->dfull), (uint32_t)(seg & 1), wc)) break;
-      tc_fence_after();
       const bool whole = (ku == 0 && seg_len == KT);
       const int m_base = mt * p.bn;
       const size_t y_col = (size_t)nt * kTileN + row;
       const long long c_first = tile_reducer(tile, KT, U, G);
       const long long c_last = stripe_owner((long long)tile * KT + KT - 1, U, G);
       const bool reducer = !whole && (long long)blockIdx.x == c_first;
+      const size_t part_stride = (size_t)p.bn * kTileN;
+      // A reducer issues its loads of the first contributor's words of its
+      // first token chunk before waiting for the accumulators, so that their
+      // round trip (about 1.5 us while other CTAs stream weights) overlaps the
+      // last MMAs (one contributor only: more pushed the kernel past its
+      // register cap).
+      uint32_t pre[8];
+      bool preloaded = false;
+      if (reducer && wg < p.bn / 8) {
+        const float* base = p.partials + (size_t)(c_first + 1) * part_stride;
+        if (W4A16_IN_RANGE(p.status, (const char*)base - (const char*)p.status, 4 * part_stride, p.ws_bytes,
+                           31)) {
+          uint32_t off[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) off[c] = (uint32_t)((wg * 8 + c) * kTileN + row);
+          issue_partials<1, 8>(base, part_stride, off, 1, pre);
+          preloaded = true;
+        }
+      }
+      if (!wait_warp(bar(ctrl->dfull), (uint32_t)(seg & 1), wc)) break;
+      tc_fence_after();
       if (reducer && dq == 0) {
         // reducer (this is its last segment): every thread polls its own words
         // of the contributors' partial tiles (a tagged word is final once
@@ -433,7 +452,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
       float* part = p.partials + (size_t)blockIdx.x * ((size_t)p.bn * kTileN);
-      const size_t part_stride = (size_t)p.bn * kTileN;
       // accumulators holding units of this tile: both, or the one of its only unit
       const bool alt = nacc == 2 && !p.split_n;
       const bool two = alt && seg_len >= 2;
@@ -459,7 +477,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t off[8];
 #pragma unroll
           for (int c = 0; c < 8; ++c) off[c] = (uint32_t)((cc * 8 + c) * kTileN + row);
-          for (long long q0 = c_first + 1; q0 <= c_last; q0 += 2) {
+          long long q0 = c_first + 1;
+          if (cc == wg && preloaded) {
+            // the first contributor, loaded before the accumulator wait (its
+            // range was checked then)
+            float* base = p.partials + (size_t)q0 * part_stride;
+            if (!poll_partials<1, 8>(base, part_stride, off, 1, pre, wc, true)) { got = false; break; }
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              acc[c] += partial_value(pre[c]);
+              __stcg(base + off[c], 0.f);
+            }
+            ++q0;
+          }
+          for (; q0 <= c_last; q0 += 2) {
             const int nq = (int)min(2LL, c_last - q0 + 1);
             float* base = p.partials + (size_t)q0 * part_stride;
             // the partial tiles of contributors q0 .. q0 + nq - 1 this thread polls
