@@ -74,10 +74,11 @@ marlin_status_t check_shape_group(int K, int N, int* group) {
 
 // Largest M served by the warp-level kernel (mma.sync fed from registers);
 // larger M uses the tcgen05 kernel.  Measured crossover (ncu, each kernel
-// forced, on 4096x12288 and 8192x8192): the warp-level kernel is 1.07-1.26x
-// faster at M <= 16, the two tie at M = 24 (tcgen05 1.01-1.02x) and the tcgen05
-// kernel is 1.12x faster at M = 32.  W4A16_SMALL_M_MAX overrides it (0..32,
-// 0 disables the warp-level path), e.g. to test either kernel at any M.
+// forced, on 4096x12288 and 8192x8192): the warp-level kernel is 1.07-1.30x
+// faster at M <= 16, the two are within 3% of each other at M = 24 (either
+// way) and the tcgen05 kernel is 1.06-1.09x faster at M = 32.
+// W4A16_SMALL_M_MAX overrides it (0..32, 0 disables the warp-level path), e.g.
+// to test either kernel at any M.
 int small_m_max() {
   static int v = [] {
     const char* e = getenv("W4A16_SMALL_M_MAX");
