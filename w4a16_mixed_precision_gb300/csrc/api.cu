@@ -209,15 +209,14 @@ GemmPlan make_plan(int M, int K, int N, int group, int sms, int smem_optin, bool
   int stages = (int)((budget - (long long)xchg) / (long long)g.stage_bytes);
   if (stages > kMaxStages) stages = kMaxStages;
   // Warp-level kernel: a ring of about 110 KB (at least 4 stages), not as many
-  // stages as fit.  Every CTA has its whole ring of weight copies in flight
-  // at once (at the start, before the dependency wait, too), and rings of
-  // 200 KB on 144 SMs queue far more than the bandwidth-latency product; the
-  // queueing delays every load behind them (the first X tile, the reducer's
-  // poll of the partial words).  Measured, graph-replayed: M = 1 on the 7B
-  // shapes 2.5-5% faster (4096x22016: 14.38 -> 13.80 us), 8192x10240 M = 1..4
-  // 3-4%, 2:4 weights at M = 1 up to 10% (4096x22016: 12.66 -> 11.38 us);
-  // M = 16 within 1% either way; 3 stages were slower again.  The tcgen05
-  // kernel keeps every stage that fits: fewer were slower at M = 32..64.
+  // stages as fit.  Every CTA keeps its whole ring of weight copies in flight
+  // (at the start, before the dependency wait, too); 110 KB on 144 SMs is
+  // still twice the bandwidth-latency product.  Measured, graph-replayed:
+  // M = 1 on the 7B shapes 2.5-5% faster (4096x22016: 14.38 -> 13.80 us),
+  // 8192x10240 M = 1..4 3-4%, 2:4 weights at M = 1 up to 10% (4096x22016:
+  // 12.66 -> 11.38 us); M = 16 within 1% either way; 3 stages were slower
+  // again.  The tcgen05 kernel keeps every stage that fits: fewer were slower
+  // at M = 32..64.
   if (g.kind == kKernelSmallM) {
     const int ring = (int)((110 * 1024) / g.stage_bytes);
     const int cap = ring > 4 ? ring : 4;
