@@ -422,9 +422,12 @@ __global__ void __launch_bounds__(kSmThreads, 1)
                     __half_as_ushort(__float2half_rn(acc[nb][d]));
             }
         } else {
-          const long long c_first = tile_reducer(tile, KT, U, G);
-          const long long c_last = stripe_owner((long long)tile * KT + KT - 1, U, G);
-          if ((long long)blockIdx.x != c_first) {
+          // The tile's reducer owns its first unit: it is this CTA exactly when
+          // the segment starts there (ku == 0; a segment starting mid-tile is
+          // the first of a contributor's stripe), so no division is needed to
+          // tell; the reducer then finds its last contributor by one.
+          const long long c_first = (long long)blockIdx.x;
+          if (ku != 0) {
             // contributor (this is its first segment): publish the partial tile
             // word by word (tagged) and go on without waiting
             float* part = p.partials + (size_t)blockIdx.x * ((size_t)p.bn * kTileN);
@@ -451,6 +454,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
             // two-block instantiations up to 6% slower (M = 16 on 8192 x 57344,
             // a code generation effect), and with it dropping the arrival
             // count saved 0.3-0.6 us per call at M <= 16 on 7B-sized shapes.
+            const long long c_last = stripe_owner((long long)tile * KT + KT - 1, U, G);
             if (g == 0) {
               if (lane == 0) {
 #ifdef MARLIN_DEBUG
