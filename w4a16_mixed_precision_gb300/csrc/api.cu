@@ -73,10 +73,11 @@ marlin_status_t check_shape_group(int K, int N, int* group) {
 }
 
 // Largest M served by the warp-level kernel (mma.sync fed from registers);
-// larger M uses the tcgen05 kernel.  Measured crossover (ncu, each kernel
-// forced, on 4096x12288 and 8192x8192): the warp-level kernel is 1.07-1.30x
-// faster at M <= 16, the two are within 3% of each other at M = 24 (either
-// way) and the tcgen05 kernel is 1.06-1.09x faster at M = 32.
+// larger M uses the tcgen05 kernel.  Measured crossover, each kernel forced,
+// calls graph-replayed on rotating weights: the warp-level kernel is
+// 1.04-1.11x faster at M = 16 (4096x12288, 8192x8192, 8192x57344), the tcgen05
+// kernel 1.03-1.11x faster at M = 24.  (Launched alone and cold under ncu, the
+// tcgen05 kernel already wins at M = 16 on 8192x8192, by 1.04x.)
 // W4A16_SMALL_M_MAX overrides it (0..32, 0 disables the warp-level path), e.g.
 // to test either kernel at any M.
 int small_m_max() {
@@ -197,6 +198,22 @@ GemmPlan make_plan(int M, int K, int N, int group, int sms, int smem_optin, bool
           g.grid = G;
           break;
         }
+      }
+      // tcgen05 kernel without an even split: a tile can have up to
+      // ceil(kt * G / units) contributors, which its reducer polls two at a
+      // time, one L2 round trip (about 1.5 us under load) each.  Take the
+      // largest grid (of at least 4/5 of the SMs) below the chosen one that
+      // needs fewer rounds, if any.  Measured: 11008x4096 at M = 32, 144 -> 128
+      // CTAs (three rounds -> two), 14.65 -> 13.26 us; every other measured
+      // shape keeps its grid (4096x12288 M = 32: one round at 144 already).
+      if (g.kind == kKernelTcgen05 && g.units % g.grid != 0) {
+        auto rounds = [&](long long G) { return ((g.kt * G + g.units - 1) / g.units + 1) / 2; };
+        const long long r0 = rounds(g.grid);
+        for (int G = g.grid - 1; G * 5 >= sms * 4; --G)
+          if (rounds(G) < r0) {
+            g.grid = G;
+            break;
+          }
       }
     }
   }

@@ -13,9 +13,10 @@ two of every four weights zero at fixed positions): the layer also holds the
 2:4 form.  marlin_sparse_gemm serves every M, but above 32 rows each further
 32-row m-tile dequantises the weights again, and on GB300 the dense tcgen05
 kernel was measured faster there (0.52-0.99x for the 2:4 path at M = 33..256
-on the Llama-2-7B shapes, against 0.98-1.15x in its favour at M = 32).  So the
-layer sends batches of up to 32 rows to marlin_sparse_gemm and larger ones to
-the dense kernel.
+on the Llama-2-7B shapes) and, since its reducer's first poll overlaps its last
+MMAs, at M = 32 too (0.97-1.00x for the 2:4 path), while the 2:4 path is
+1.12-1.27x faster at M <= 16.  So the layer sends batches of up to 16 rows to
+marlin_sparse_gemm and larger ones to the dense kernel.
 """
 from __future__ import annotations
 
@@ -29,14 +30,17 @@ from .formats import awq_to_gptq
 class W4A16Linear(torch.nn.Module):
     """y[..., N] = x[..., K] . dequant(W)[K, N], fp16 in and out, fp32 accumulation."""
 
-    SPARSE_MAX_M = 32  # largest batch sent to the 2:4 path (above it the dense kernel measured faster)
+    # Largest batch sent to the 2:4 path.  Measured on the 7B shapes: 1.12-1.27x
+    # faster than the dense call at M <= 16, 0.97-1.00x at M = 32 (where the
+    # dense call runs the tcgen05 kernel).
+    SPARSE_MAX_M = 16
 
     def __init__(self, qweight: torch.Tensor, scales: torch.Tensor, qzeros: torch.Tensor | None = None,
                  group: int = 128, device=None, sparse: bool = False):
         """qweight: GPTQ-order int32 [K/8, N]; scales fp16 [K/group, N]; qzeros
         int32 [K/group, N/8] or None (z = 8); group 128, a multiple of 128
         dividing K, or -1/K for one scale per column.  sparse: the weights are
-        2:4 (raises otherwise); batches of M <= 32 use the sparse path."""
+        2:4 (raises otherwise); batches of M <= SPARSE_MAX_M use the sparse path."""
         super().__init__()
         dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
         q = qweight.to(dev, torch.int32).contiguous()
