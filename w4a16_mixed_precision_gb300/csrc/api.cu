@@ -373,6 +373,7 @@ marlin_status_t run_gemm(const uint16_t* X, const void* packed, const void* meta
   p.timeout_ns = kDefaultTimeoutNs;
   p.early_weights = early_weights() ? 1 : 0;
   p.x3d = g.bn <= 64 ? 1 : 0;
+  p.even_split = (g.units % g.grid == 0 && g.kt % (g.units / g.grid) == 0) ? 1 : 0;
   // extents for the bounds-checked build: the logical sizes of the caller's buffers
   {
     const size_t Gr = (size_t)(K / group);

@@ -45,6 +45,7 @@ struct Ctrl {
   uint64_t dempty;
   uint64_t drain[2];
   uint64_t red_go;      // leader -> dequant warps: the reducer may write Y
+  uint64_t red_copy;    // the reducer's bulk copies of its contributors' partial tiles landed
   uint32_t tmem_base;
   int abort;
 };
@@ -63,7 +64,11 @@ static_assert(kThreads == 32 * (kFirstDqWarp + kNumDqWarps), "block size");
 // on their path sits directly on the critical path of the whole CTA.
 
 // ZP: explicit zero points (else the implicit zero 8 folds into constants).
-template <bool ZP>
+// BULK: bn > 32, where a warpgroup's epilogue covers several token chunks: a
+// reducer may copy its contributors' partial tiles into the drained ring in
+// bulk instead of polling them chunk by chunk (separate instantiation, so that
+// the bn <= 32 plans keep the code generated without it).
+template <bool ZP, bool BULK>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_gemm_kernel(const __grid_constant__ CUtensorMap x_map, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -107,6 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(ctrl->drain[0]), 1);
     mbar_init(bar(ctrl->drain[1]), 1);
     mbar_init(bar(ctrl->red_go), 1);
+    mbar_init(bar(ctrl->red_copy), 1);
     ctrl->abort = 0;
     fence_mbarrier_init();
   }
@@ -451,6 +457,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
+      // BULK: a reducer whose warpgroups would otherwise wait for more than one
+      // exposed round trip (about 1.5 us each while other CTAs stream weights:
+      // one per token chunk and pair of contributors, the first hidden by the
+      // load issued ahead) copies its contributors' partial tiles into the
+      // ring, free now that the accumulators are final, with one bulk copy
+      // each, and reads every chunk's words from there.  A word still zero in
+      // the copy (its contributor not done) is polled from global memory.  Not
+      // on an even split, where every contributor finishes its piece together
+      // with the reducer (measured: the copy then mostly comes too early, and
+      // 8192x8192 at M = 128 was 0.5 us slower with it).
+      const uint32_t tile_bytes = (uint32_t)(part_stride * sizeof(float));
+      int n_copy = 0;
+      if constexpr (BULK) {
+        if (reducer) {
+          const long long nc = c_last - c_first;
+          const long long cpw = (p.bn / 8 + kNumDqWG - 1) / kNumDqWG;  // token chunks per warpgroup
+          const long long exposed = cpw * ((nc + 1) / 2) - (preloaded ? 1 : 0);
+          const long long fit = (long long)((size_t)S * p.stage_bytes / tile_bytes);
+          n_copy = (exposed > 1 && !p.even_split) ? (int)min(fit, nc) : 0;
+          const float* src = p.partials + (size_t)(c_first + 1) * part_stride;
+          if (n_copy > 0 &&
+              (!W4A16_IN_RANGE(p.status, (const char*)src - (const char*)p.status,
+                               (size_t)n_copy * tile_bytes, p.ws_bytes, 31) ||
+               !W4A16_SMEM_OK(p, raw_addr, stage0, (uint32_t)n_copy * tile_bytes, 33)))
+            n_copy = 0;
+          if (n_copy > 0) {
+            if (dq == 0 && lane == 0) {
+              fence_proxy_async_smem();
+              mbar_arrive_expect_tx(bar(ctrl->red_copy), (uint32_t)n_copy * tile_bytes);
+              for (int i = 0; i < n_copy; ++i)
+                bulk_g2s(stage0 + (uint32_t)i * tile_bytes, src + (size_t)i * part_stride, tile_bytes,
+                         bar(ctrl->red_copy), policy_evict_first());
+            }
+            if (!wait_warp(bar(ctrl->red_copy), 0, wc)) {
+              if (dq == 0 && lane == 0) wait_drain(bar(ctrl->red_copy), 0, wc);  // the copies land before exit
+              break;
+            }
+          }
+        }
+      }
       float* part = p.partials + (size_t)blockIdx.x * ((size_t)p.bn * kTileN);
       // accumulators holding units of this tile: both, or the one of its only unit
       const bool alt = nacc == 2 && !p.split_n;
@@ -490,23 +536,55 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++q0;
           }
-          for (; q0 <= c_last; q0 += 2) {
-            const int nq = (int)min(2LL, c_last - q0 + 1);
-            float* base = p.partials + (size_t)q0 * part_stride;
-            // the partial tiles of contributors q0 .. q0 + nq - 1 this thread polls
-            if (!W4A16_IN_RANGE(p.status, (const char*)base - (const char*)p.status,
-                                4 * (size_t)nq * part_stride, p.ws_bytes, 31)) { got = false; break; }
-            uint32_t raw[16];
-            if (!poll_partials<2, 8>(base, part_stride, off, nq, raw, wc)) { got = false; break; }
+          if constexpr (BULK) {
+            for (; q0 <= c_first + n_copy; ++q0) {
+              // a contributor copied in bulk: its words from the ring
+              const uint32_t sb = stage0 + (uint32_t)(q0 - c_first - 1) * tile_bytes;
+              float* base = p.partials + (size_t)q0 * part_stride;
+              uint32_t raw[8];
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
-              if (j < nq) {
+              for (int c = 0; c < 8; ++c) raw[c] = lds_u32(sb + 4u * off[c]);
+              if (!poll_partials<1, 8>(base, part_stride, off, 1, raw, wc, true)) { got = false; break; }
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                  acc[c] += partial_value(raw[j * 8 + c]);
-                  __stcg(base + j * part_stride + off[c], 0.f);
-                }
+              for (int c = 0; c < 8; ++c) {
+                acc[c] += partial_value(raw[c]);
+                __stcg(base + off[c], 0.f);
               }
+            }
+          }
+          if constexpr (BULK) {
+            for (; q0 <= c_last && got; ++q0) {
+              // contributors beyond the ring's room: polled from global memory
+              float* base = p.partials + (size_t)q0 * part_stride;
+              if (!W4A16_IN_RANGE(p.status, (const char*)base - (const char*)p.status, 4 * part_stride,
+                                  p.ws_bytes, 31)) { got = false; break; }
+              uint32_t raw[8];
+              if (!poll_partials<1, 8>(base, part_stride, off, 1, raw, wc)) { got = false; break; }
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                acc[c] += partial_value(raw[c]);
+                __stcg(base + off[c], 0.f);
+              }
+            }
+          } else {
+            for (; q0 <= c_last && got; q0 += 2) {
+              const int nq = (int)min(2LL, c_last - q0 + 1);
+              float* base = p.partials + (size_t)q0 * part_stride;
+              // the partial tiles of contributors q0 .. q0 + nq - 1 this thread polls
+              if (!W4A16_IN_RANGE(p.status, (const char*)base - (const char*)p.status,
+                                  4 * (size_t)nq * part_stride, p.ws_bytes, 31)) { got = false; break; }
+              uint32_t raw[16];
+              if (!poll_partials<2, 8>(base, part_stride, off, nq, raw, wc)) { got = false; break; }
+#pragma unroll
+              for (int j = 0; j < 2; ++j)
+                if (j < nq) {
+#pragma unroll
+                  for (int c = 0; c < 8; ++c) {
+                    acc[c] += partial_value(raw[j * 8 + c]);
+                    __stcg(base + j * part_stride + off[c], 0.f);
+                  }
+                }
+            }
           }
           if (!got) break;
           if (!go_seen) {
@@ -554,10 +632,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t gemm_set_smem_limit(int bytes) {
-  cudaError_t e = cudaFuncSetAttribute(w4a16_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       bytes);
+  cudaError_t e = cudaFuncSetAttribute(w4a16_gemm_kernel<false, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(w4a16_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = cudaFuncSetAttribute(w4a16_gemm_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(w4a16_gemm_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(w4a16_gemm_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   return e;
 }
 
@@ -573,8 +655,12 @@ cudaError_t launch_gemm(const CUtensorMap& x_map, const GemmParams& p, int grid,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (p.zeros) return cudaLaunchKernelEx(&cfg, w4a16_gemm_kernel<true>, x_map, p);
-  return cudaLaunchKernelEx(&cfg, w4a16_gemm_kernel<false>, x_map, p);
+  const bool bulk = p.bn > 32;
+  if (p.zeros)
+    return bulk ? cudaLaunchKernelEx(&cfg, w4a16_gemm_kernel<true, true>, x_map, p)
+                : cudaLaunchKernelEx(&cfg, w4a16_gemm_kernel<true, false>, x_map, p);
+  return bulk ? cudaLaunchKernelEx(&cfg, w4a16_gemm_kernel<false, true>, x_map, p)
+              : cudaLaunchKernelEx(&cfg, w4a16_gemm_kernel<false, false>, x_map, p);
 }
 
 }  // namespace w4a16

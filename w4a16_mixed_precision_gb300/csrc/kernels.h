@@ -63,6 +63,7 @@ struct GemmParams {
   uint32_t a_base;          // tcgen05 kernel: TMEM column of A slot 0 (accumulators below it)
   int early_weights;        // stream the first ring of weights before the dependency wait
   int x3d;                  // X tensor map is [K/64][M][64] with a box of one unit's cpu chunks
+  int even_split;           // every CTA holds the same whole number of units and every tile splits evenly
   unsigned long long timeout_ns;
   // Extents the bounds-checked (MARLIN_DEBUG) build checks addresses against,
   // in bytes: the logical sizes of the buffers the caller passed, and the

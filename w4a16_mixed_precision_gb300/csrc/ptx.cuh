@@ -55,6 +55,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity,
   return ok != 0;
 }
 
+// Orders this thread's earlier generic-proxy accesses to shared memory before
+// its later async-proxy (TMA) accesses to it.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---- TMA (bulk and tensor copies, global -> shared) ---------------------------
 
 __device__ __forceinline__ uint64_t policy_evict_first() {
