@@ -55,6 +55,11 @@ SMALL_CASES = [
     (1, 128, 128, 128, True),          # one unit, one tile, explicit zeros
     (40, 128, 256, 128, False),        # K of a single 128-row unit on the tcgen05 kernel
     (600, 1024, 512, 128, False),
+    # more units than SMs, split unevenly (140 CTAs on 152 SMs: up to 15 pieces per tile):
+    # the tcgen05 reducer copies its first contributors' partial tiles in bulk and
+    # polls the rest
+    (128, 4096, 1280, 128, False),
+    (64, 4096, 1280, 128, True),
 ]
 
 
